@@ -1,0 +1,561 @@
+"""Benchmark of the MSA forward on one GB300 (or N independent replicas).
+
+Headline workload: flat varlen prefill, 2 sequences x 32768 tokens, 64 query /
+8 KV heads, head_dim 128, bf16, causal, top-16 of 128-token blocks per query
+(diagonal, first and previous block plus random visible blocks). One step is
+one pass of the forward (union metadata + sparse attention) over that batch.
+
+value       effective TFLOP/s = 4 * d * sum over (query, head) of the visible
+            keys in its selected blocks, divided by the device time per step
+e2e         the same metric through the public API with host buffers: pinned
+            host -> device copies of the step's inputs, the call, and the
+            device -> host copy of out and lse, all inside the timed region
+roofline    the attention kernel alone (CUDA events the library records on the
+            launching stream between its own launches) against the measured
+            bf16 tensor peak
+cpu_baseline  the fp64 CPU oracle on a bounded row sample of the same workload
+decode / two_stage  secondary measurements on the paged-decode workload
+            (KV GB/s vs HBM) and on the two-stage proxy -> top-k -> attention
+            pipeline, each kernel timed alone with L2 flushed between launches
+
+``--impl reference`` times the oracle itself (host cores) on a bounded sample.
+Under torchrun with N > 1 every rank runs the same workload on its own GPU
+(replicas; no collective on the data path) and the step time is the max over
+ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "MSA fwd TFLOP/s (prefill) and KV GB/s (decode) vs GB300 roofline, 1 GPU"
+D = 128
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- measurement helpers
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        loaded = [x for x in sm if x >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def l2_flush_buffer(device):
+    return torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+
+def time_launch(fn, device, reps=5, flush=None):
+    """Median device time (s) of fn() over reps launches, L2 flushed before each."""
+    times = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.fill_(1)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        torch.cuda.synchronize(device)
+        times.append(s.elapsed_time(e) * 1e-3)
+    return statistics.median(times)
+
+
+# ---------------------------------------------------------------- work accounting
+def visible_counts(q2k, cu_q, k_lens, causal=True):
+    """Per (kv head, query): visible keys in its distinct selected blocks."""
+    dev = q2k.device
+    hkv, tq, topk = q2k.shape
+    cu = cu_q.cpu().tolist()
+    pos = workloads.query_positions(cu_q.cpu(), k_lens).to(dev)
+    lk = torch.cat([torch.full((cu[b + 1] - cu[b],), int(k_lens[b]), dtype=torch.int64)
+                    for b in range(len(cu) - 1)]).to(dev)
+    ids = q2k.long()
+    srt, _ = torch.sort(torch.where(ids >= 0, ids, torch.full_like(ids, 1 << 40)), dim=-1)
+    dup = torch.zeros_like(srt, dtype=torch.bool)
+    dup[..., 1:] = srt[..., 1:] == srt[..., :-1]
+    lim = torch.minimum(lk, pos + 1) if causal else lk
+    start = srt * 128
+    n = torch.clamp(torch.minimum(lim[None, :, None] - start, torch.full_like(start, 128)), min=0)
+    n = torch.where((srt < (1 << 40)) & ~dup, n, torch.zeros_like(n))
+    return n.sum(-1)  # (hkv, tq)
+
+
+# ---------------------------------------------------------------- headline: flat prefill
+def prefill_inputs(device, seed=0):
+    spec = workloads.FLAT_VARLEN
+    inp = workloads.make_prefill(spec, seed, device=device)
+    return spec, inp
+
+
+def run_prefill(msa, inp, out, lse, ws, max_sq):
+    return msa.msa_sparse_attention_fwd(
+        inp["q"], inp["k"], inp["v"], inp["q2k_indices"], inp["cu_seqlens_q"],
+        inp["cu_seqlens_k"], causal=True, softmax_scale=inp["softmax_scale"],
+        max_seqlen_q=max_sq, out=out, lse=lse, workspace=ws)
+
+
+def cpu_baseline_prefill(inp, rows_target=512, threads=None):
+    """fp64 oracle on a bounded row sample; returns (TFLOP/s, cores, sample, seconds)."""
+    import oracle
+    cpu = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    tq = cpu["q"].shape[0]
+    g = torch.Generator().manual_seed(1234)
+    rows = torch.sort(torch.randperm(tq, generator=g)[:rows_target])[0].to(torch.int32)
+    hkv = cpu["k"].shape[1]
+    G = cpu["q"].shape[1] // hkv
+    cnt = visible_counts(cpu["q2k_indices"], cpu["cu_seqlens_q"], cpu["lengths"])
+    flops = 4.0 * D * G * float(cnt[:, rows.long()].sum())
+    cores = threads or os.cpu_count() or 1
+    scale = float(np.float32(inp["softmax_scale"]))
+    oracle.sparse_attention(cpu["q"], cpu["k"], cpu["v"], cpu["q2k_indices"],
+                            cpu["cu_seqlens_q"], cpu["cu_seqlens_k"], causal=True,
+                            softmax_scale=scale, rows=rows[:8], threads=cores)  # warm
+    t0 = time.perf_counter()
+    oracle.sparse_attention(cpu["q"], cpu["k"], cpu["v"], cpu["q2k_indices"],
+                            cpu["cu_seqlens_q"], cpu["cu_seqlens_k"], causal=True,
+                            softmax_scale=scale, rows=rows, threads=cores)
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, cores, f"{len(rows)} of {tq} query rows x all {cpu['q'].shape[1]} heads", dt
+
+
+def bench_prefill(msa, args, device, world, rank):
+    spec, inp = prefill_inputs(device)
+    tq, hq, _ = inp["q"].shape
+    hkv = inp["k"].shape[1]
+    G = hq // hkv
+    max_sq = max(inp["lengths"])
+    cnt = visible_counts(inp["q2k_indices"], inp["cu_seqlens_q"], inp["lengths"])
+    flops = 4.0 * D * G * float(cnt.sum())
+    blocks = (inp["q2k_indices"] >= 0).sum().item()
+    flops_block = 4.0 * D * G * 128 * float(blocks)
+    out = torch.empty_like(inp["q"])
+    lse = torch.empty((tq, hq), dtype=torch.float32, device=device)
+    need = msa.msa_sparse_attention_workspace_size(len(inp["lengths"]), tq, hq, hkv, D, 16,
+                                                   max_sq, False)
+    ws = torch.empty(need, dtype=torch.uint8, device=device)
+    # Executed MMA work: union blocks per 128-row tile (same W as the forward).
+    W = msa.msa_union_tile_tokens(hq, hkv)
+    ulen = msa.msa_build_union(inp["q2k_indices"], inp["cu_seqlens_q"], inp["cu_seqlens_k"],
+                               causal=True, tile_tokens=W)[0]
+    union_blocks = float(ulen.sum().item())
+    flops_exec = union_blocks * 4.0 * D * 128 * 128
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        run_prefill(msa, inp, out, lse, ws, max_sq)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize(device)
+        barrier(world)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for i in range(args.steps):
+            msa.msa_set_timing_events(evs[i])  # host-side only: which events to record
+            run_prefill(msa, inp, out, lse, ws, max_sq)
+        end.record()
+        torch.cuda.synchronize(device)
+        msa.msa_set_timing_events(None)
+        barrier(world)
+    wall = start.elapsed_time(end) * 1e-3
+    meta_times = [e[0].elapsed_time(e[1]) * 1e-3 for e in evs]
+    attn_times = [e[1].elapsed_time(e[2]) * 1e-3 for e in evs]
+    step_s = max_over_ranks(wall / args.steps, world, device if world > 1 else None)
+    attn_s = statistics.mean(attn_times)
+    fault = msa.msa_read_device_fault()
+    pk = peaks()
+    achieved = flops / attn_s / 1e12
+    res = dict(
+        spec=spec, inp=inp, flops=flops, flops_block=flops_block, flops_exec=flops_exec,
+        step_s=step_s, wall_s=wall, attn_s=attn_s, meta_s=statistics.mean(meta_times),
+        value=aggregate_value(flops, world, step_s) / 1e12, clocks=clk.summary(), fault=fault,
+        roofline={"bound": "tensor", "achieved": round(achieved, 2),
+                  "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                  "frac": round(achieved / pk["bf16_sus"], 4), "traffic": None,
+                  "kernel": "prefill_kernel<bf16>",
+                  "peak_kind": f"bf16_tflops_sustained ({pk['source']})",
+                  "achieved_is": "algorithmic FLOP per launch / mean launch time"},
+        executed_tflops=flops_exec / attn_s / 1e12,
+        work_efficiency=flops / flops_exec,
+        union_blocks_per_tile=union_blocks / ulen.numel(),
+    )
+    # End-to-end through the public API with host buffers.
+    host = {k: v.cpu().pin_memory() for k, v in inp.items()
+            if torch.is_tensor(v) and k in ("q", "k", "v", "q2k_indices", "cu_seqlens_q",
+                                            "cu_seqlens_k")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dev_bufs = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def e2e_step():
+        for k2, v2 in host.items():
+            dev_bufs[k2].copy_(v2, non_blocking=True)
+        d = dict(dev_bufs, softmax_scale=inp["softmax_scale"])
+        run_prefill(msa, d, out, lse, ws, max_sq)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(device)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    n_e2e = max(3, min(args.steps, 10))
+    for _ in range(n_e2e):
+        e2e_step()
+    e.record()
+    torch.cuda.synchronize(device)
+    e2e_s = s.elapsed_time(e) * 1e-3 / n_e2e
+    e2e_s = max_over_ranks(e2e_s, world, device if world > 1 else None)
+    res["e2e"] = {"value": round(aggregate_value(flops, world, e2e_s) / 1e12, 3),
+                  "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
+                  "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_s * 1e3, 3)}
+    return res
+
+
+# ---------------------------------------------------------------- secondary: paged decode
+def bench_decode(msa, device, flush, seed=0):
+    spec = workloads.PAGED_DECODE
+    out = {}
+    pk = peaks()
+    for sq in (1, 4):
+        inp = workloads.make_decode(spec, seed, device=device, seqlen_q=sq)
+        q2k, pt, su = inp["q2k_indices"], inp["page_table"], inp["seqused_k"]
+        hkv = inp["k"].shape[1]
+        G = inp["q"].shape[1] // hkv
+        # Distinct valid K+V bytes of each (request, KV head)'s union of pages.
+        B = pt.shape[0]
+        ids = q2k.view(hkv, B, sq * q2k.shape[2]).long()
+        lens = su.long()
+        srt, _ = torch.sort(torch.where(ids >= 0, ids, torch.full_like(ids, 1 << 40)), dim=-1)
+        first = torch.ones_like(srt, dtype=torch.bool)
+        first[..., 1:] = srt[..., 1:] != srt[..., :-1]
+        valid = torch.clamp(torch.minimum(lens[None, :, None] - srt * 128,
+                                          torch.full_like(srt, 128)), min=0)
+        valid = torch.where((srt < (1 << 40)) & first, valid, torch.zeros_like(valid))
+        kv_bytes = float(valid.sum()) * D * 2 * 2
+        meta = (inp["q"].numel() * 2 * 2 + inp["q"].shape[0] * inp["q"].shape[1] * 4 +
+                q2k.numel() * 4 + pt.numel() * 4)
+        o = torch.empty_like(inp["q"])
+        lse = torch.empty(inp["q"].shape[:2], dtype=torch.float32, device=device)
+        need = msa.msa_sparse_attention_workspace_size(B, inp["q"].shape[0], inp["q"].shape[1],
+                                                       hkv, D, q2k.shape[2], sq, True)
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+
+        def call():
+            msa.msa_sparse_attention_fwd(inp["q"], inp["k"], inp["v"], q2k, inp["cu_seqlens_q"],
+                                         None, causal=True, page_table=pt, seqused_k=su,
+                                         max_seqlen_q=sq, out=o, lse=lse, workspace=ws)
+
+        for _ in range(3):
+            call()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ts = []
+        for _ in range(7):
+            flush.fill_(1)
+            msa.msa_set_timing_events(ev)
+            call()
+            ev[2].synchronize()
+            ts.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+        msa.msa_set_timing_events(None)
+        t = statistics.median(ts)
+        gbs = (kv_bytes + meta) / t / 1e9
+        out[f"seqlen_q_{sq}"] = {
+            "value": round(gbs, 1), "unit": "GB/s", "us": round(t * 1e6, 2),
+            "kv_bytes": int(kv_bytes), "meta_bytes": int(meta),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4), "traffic": None,
+                         "kernel": "decode_kernel"}}
+        del inp
+        torch.cuda.empty_cache()
+    out["workload"] = spec.name
+    return out
+
+
+# ---------------------------------------------------------------- secondary: two-stage
+def bench_two_stage(msa, device, flush, seed=0):
+    spec = workloads.TWO_STAGE
+    inp = workloads.make_two_stage(spec, seed, device=device)
+    L = spec.seqlens[0]
+    T = (L + 127) // 128
+    pk = peaks()
+    scores = torch.empty((1, T, L), dtype=torch.float32, device=device)
+    q2k = torch.empty((spec.num_kv_heads, L, spec.topk), dtype=torch.int32, device=device)
+    res = {"workload": spec.name}
+
+    def proxy():
+        msa.msa_proxy_score(inp["proxy_q"], inp["index_k"], inp["cu_seqlens_q"],
+                            inp["cu_seqlens_k"], causal=True, max_k_tiles=T, reduce_heads=True,
+                            output=scores)
+
+    def topk():
+        msa.msa_topk_select(scores, spec.topk, spec.num_kv_heads, out=q2k)
+
+    proxy()
+    topk()
+    t_proxy = time_launch(proxy, device, reps=3, flush=flush)
+    t_topk = time_launch(topk, device, reps=5, flush=flush)
+    pflops = 2.0 * D * spec.proxy_heads * L * (L + 1) / 2
+    res["proxy"] = {"tflops": round(pflops / t_proxy / 1e12, 2), "ms": round(t_proxy * 1e3, 3),
+                    "frac_of_bf16_peak": round(pflops / t_proxy / 1e12 / pk["bf16"], 4)}
+    tk_bytes = scores.numel() * 4 + q2k.numel() * 4
+    res["topk"] = {"gbs": round(tk_bytes / t_topk / 1e9, 1), "us": round(t_topk * 1e6, 2),
+                   "frac_of_hbm": round(tk_bytes / t_topk / 1e9 / pk["hbm"], 4)}
+    out = torch.empty_like(inp["q"])
+    lse = torch.empty(inp["q"].shape[:2], dtype=torch.float32, device=device)
+    need = msa.msa_sparse_attention_workspace_size(1, L, spec.num_qo_heads, spec.num_kv_heads, D,
+                                                   spec.topk, L, False)
+    ws = torch.empty(need, dtype=torch.uint8, device=device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def attn():
+        msa.msa_sparse_attention_fwd(inp["q"], inp["k"], inp["v"], q2k, inp["cu_seqlens_q"],
+                                     inp["cu_seqlens_k"], causal=True, max_seqlen_q=L, out=out,
+                                     lse=lse, workspace=ws)
+
+    attn()
+    ts = []
+    for _ in range(3):
+        flush.fill_(1)
+        msa.msa_set_timing_events(ev)
+        attn()
+        ev[2].synchronize()
+        ts.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+    msa.msa_set_timing_events(None)
+    t_attn = statistics.median(ts)
+    G = spec.num_qo_heads // spec.num_kv_heads
+    cnt = visible_counts(q2k, inp["cu_seqlens_q"], spec.seqlens)
+    aflops = 4.0 * D * G * float(cnt.sum())
+    res["attention"] = {"tflops": round(aflops / t_attn / 1e12, 2), "ms": round(t_attn * 1e3, 3),
+                        "frac_of_bf16_peak": round(aflops / t_attn / 1e12 / pk["bf16"], 4)}
+    res["pipeline_ms"] = round((t_proxy + t_topk + t_attn) * 1e3, 3)
+    return res
+
+
+# ---------------------------------------------------------------- reference arm: the oracle
+def reference_arm(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    spec = workloads.FLAT_VARLEN
+    inp = workloads.make_prefill(spec, 0, device="cpu")
+    tq = inp["q"].shape[0]
+    hkv = inp["k"].shape[1]
+    G = inp["q"].shape[1] // hkv
+    cnt = visible_counts(inp["q2k_indices"], inp["cu_seqlens_q"], inp["lengths"])
+    cores = os.cpu_count() or 1
+    rows_per_step = 64
+    g = torch.Generator().manual_seed(77)
+    scale = float(np.float32(inp["softmax_scale"]))
+    times, flops = [], []
+    for step in range(args.warmup + args.steps):
+        rows = torch.sort(torch.randperm(tq, generator=g)[:rows_per_step])[0].to(torch.int32)
+        f = 4.0 * D * G * float(cnt[:, rows.long()].sum())
+        t0 = time.perf_counter()
+        oracle.sparse_attention(inp["q"], inp["k"], inp["v"], inp["q2k_indices"],
+                                inp["cu_seqlens_q"], inp["cu_seqlens_k"], causal=True,
+                                softmax_scale=scale, rows=rows, threads=cores)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            flops.append(f)
+    v = sum(flops) / sum(times) / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": spec.name, "global_batch": 2, "seq_len": 32768,
+                       "parallelism": "none (host cores)"},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{rows_per_step} random query rows x all heads per step"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="msa", choices=["msa", "reference"])
+    ap.add_argument("--no-secondary", action="store_true", help="skip decode / two-stage")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    import block_sparse_top_msa_gb300 as msa
+    msa.build()
+    res = bench_prefill(msa, args, device, world, rank)
+    flush = l2_flush_buffer(device)
+    secondary = {}
+    if not args.no_secondary and rank == 0:
+        inp_keep = res.pop("inp")
+        del inp_keep
+        torch.cuda.empty_cache()
+        secondary["decode"] = bench_decode(msa, device, flush)
+        torch.cuda.empty_cache()
+        secondary["two_stage"] = bench_two_stage(msa, device, flush)
+    else:
+        res.pop("inp")
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        _, inp_cpu = prefill_inputs(device)
+        v, cores, sample, dt = cpu_baseline_prefill(inp_cpu)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": sample, "seconds": round(dt, 2)}
+    if rank == 0:
+        spec = res["spec"]
+        line = {
+            "metric": METRIC, "value": round(res["value"], 3), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(res["step_s"] * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": spec.name, "global_batch": 2 * world, "seq_len": 32768,
+                       "num_qo_heads": 64, "num_kv_heads": 8, "head_dim": 128, "topk": 16,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (q 1.07 GB, k+v 268 MB, out 1.07 GB per step)"},
+            "roofline": res["roofline"],
+            "cpu_baseline": cpu,
+            "e2e": res["e2e"],
+            "gpu_launches": 2 * args.steps,
+            "clocks": res["clocks"],
+            "work": {"algorithmic_tflop": round(res["flops"] / 1e12, 4),
+                     "block_granular_tflop": round(res["flops_block"] / 1e12, 4),
+                     "executed_mma_tflop": round(res["flops_exec"] / 1e12, 4),
+                     "work_efficiency": round(res["work_efficiency"], 4),
+                     "executed_mma_tflops": round(res["executed_tflops"], 2),
+                     "union_blocks_per_tile": round(res["union_blocks_per_tile"], 2),
+                     "attention_ms": round(res["attn_s"] * 1e3, 3),
+                     "metadata_ms": round(res["meta_s"] * 1e3, 3)},
+            "device_fault_word": res["fault"],
+        }
+        line.update(secondary)
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

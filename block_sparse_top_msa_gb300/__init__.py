@@ -1,0 +1,262 @@
+"""MiniMax Sparse Attention (MSA) forward on GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libmsa.so`` (declared in
+``include/msa.h``). Every function here only marshals torch CUDA tensors into
+raw device pointers and sizes and calls the C entry point of the same name;
+all computation happens in the library's CUDA kernels. There is no fallback:
+if the library has not been built, every call raises.
+
+Convenience defaults that need information the C ABI takes explicitly
+(``max_seqlen_q``, ``max_k_tiles``) are derived here from ``cu_seqlens``,
+which costs one device-to-host copy; pass them to avoid it. Output and
+workspace buffers are allocated with torch when not supplied.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmsa.so")
+
+MSA_OK, MSA_INVALID_ARG, MSA_UNSUPPORTED, MSA_WORKSPACE_TOO_SMALL, MSA_CUDA_ERROR = range(5)
+MSA_BF16, MSA_FP16, MSA_FP8_E4M3 = 0, 1, 2
+
+_lib = None
+
+
+class MSAError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+def build(force: bool = False) -> str:
+    """Compile libmsa.so in-tree with nvcc (sm_103a)."""
+    from . import buildlib as _b
+    return _b.build(force=force)
+
+
+def lib():
+    """The loaded C library. Raises if it was never built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libmsa.so is not built ({LIB_PATH}); run "
+                "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        L = C.CDLL(LIB_PATH)
+        vp, i32, f32, sz = C.c_void_p, C.c_int, C.c_float, C.c_size_t
+        L.msa_status_string.restype = C.c_char_p
+        L.msa_status_string.argtypes = [i32]
+        L.msa_sparse_attention_workspace_size.restype = sz
+        L.msa_sparse_attention_workspace_size.argtypes = [i32] * 8
+        L.msa_sparse_attention_fwd.restype = i32
+        L.msa_sparse_attention_fwd.argtypes = [
+            vp, i32, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, vp, i32, i32, i32, i32, i32,
+            i32, i32, i32, f32, vp, vp, vp, sz, vp]
+        L.msa_proxy_score.restype = i32
+        L.msa_proxy_score.argtypes = [
+            vp, i32, vp, i32, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+            i32, vp, vp]
+        L.msa_topk_select.restype = i32
+        L.msa_topk_select.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp]
+        L.msa_build_union.restype = i32
+        L.msa_build_union.argtypes = [
+            vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+        L.msa_union_tile_tokens.restype = i32
+        L.msa_union_tile_tokens.argtypes = [i32, i32]
+        L.msa_set_timing_events.restype = i32
+        L.msa_set_timing_events.argtypes = [C.POINTER(C.c_void_p), i32]
+        L.msa_read_device_fault.restype = i32
+        L.msa_read_device_fault.argtypes = [C.POINTER(C.c_uint), vp]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().msa_status_string(int(status)).decode()
+
+
+def _check(fn, status):
+    if status != MSA_OK:
+        raise MSAError(fn, status)
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return MSA_BF16
+    if t.dtype == torch.float16:
+        return MSA_FP16
+    if t.dtype in (torch.float8_e4m3fn, torch.uint8):
+        return MSA_FP8_E4M3
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _cuda_contig(name, t, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def _max_len(cu: torch.Tensor) -> int:
+    return int((cu[1:] - cu[:-1]).max().item()) if cu.numel() > 1 else 0
+
+
+def msa_union_tile_tokens(num_qo_heads: int, num_kv_heads: int) -> int:
+    return int(lib().msa_union_tile_tokens(num_qo_heads, num_kv_heads))
+
+
+def msa_sparse_attention_workspace_size(batch, total_q, num_qo_heads, num_kv_heads, head_dim,
+                                        topk, max_seqlen_q, paged) -> int:
+    return int(lib().msa_sparse_attention_workspace_size(
+        batch, total_q, num_qo_heads, num_kv_heads, head_dim, topk, max_seqlen_q, int(bool(paged))))
+
+
+def msa_sparse_attention_fwd(q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k=None, *,
+                             causal=False, softmax_scale=None, page_table=None, seqused_k=None,
+                             max_seqlen_q=None, return_softmax_lse=False, out=None, lse=None,
+                             workspace=None, stream=None):
+    """Sparse attention forward; see ``msa_sparse_attention_fwd`` in include/msa.h.
+
+    Returns ``out`` or ``(out, lse)``.
+    """
+    L = lib()
+    _cuda_contig("q", q)
+    _cuda_contig("k", k)
+    _cuda_contig("v", v)
+    _cuda_contig("q2k_indices", q2k_indices, torch.int32)
+    _cuda_contig("cu_seqlens_q", cu_seqlens_q, torch.int32)
+    _cuda_contig("cu_seqlens_k", cu_seqlens_k, torch.int32)
+    _cuda_contig("page_table", page_table, torch.int32)
+    _cuda_contig("seqused_k", seqused_k, torch.int32)
+    total_q, hq, d = q.shape
+    hkv = k.shape[1]
+    topk = q2k_indices.shape[2]
+    batch = cu_seqlens_q.shape[0] - 1
+    paged = page_table is not None
+    if max_seqlen_q is None:
+        max_seqlen_q = _max_len(cu_seqlens_q)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_softmax_lse:
+        lse = torch.empty((total_q, hq), dtype=torch.float32, device=q.device)
+    need = msa_sparse_attention_workspace_size(batch, total_q, hq, hkv, d, topk,
+                                               max(1, max_seqlen_q), paged)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    st = L.msa_sparse_attention_fwd(
+        _p(q), _dtype_code(q), _p(k), _p(v), _dtype_code(k), _p(q2k_indices), topk,
+        _p(cu_seqlens_q), _p(cu_seqlens_k), _p(page_table),
+        page_table.shape[1] if paged else 0, k.shape[0] if paged else 0, _p(seqused_k), batch,
+        total_q, 0 if paged else k.shape[0], hq, hkv, d, int(max_seqlen_q), int(bool(causal)),
+        float(softmax_scale) if softmax_scale is not None else 0.0, _p(out), _p(lse),
+        _p(workspace), workspace.numel(), _stream(stream))
+    _check("msa_sparse_attention_fwd", st)
+    return (out, lse) if lse is not None else out
+
+
+def msa_proxy_score(q, k, cu_seqlens_q, cu_seqlens_k, *, causal=True, max_k_tiles=None,
+                    reduce_heads=False, output=None, max_seqlen_q=None, stream=None):
+    """Per-block max of unscaled causal q.k; see ``msa_proxy_score`` in include/msa.h."""
+    L = lib()
+    _cuda_contig("q", q)
+    _cuda_contig("k", k)
+    _cuda_contig("cu_seqlens_q", cu_seqlens_q, torch.int32)
+    _cuda_contig("cu_seqlens_k", cu_seqlens_k, torch.int32)
+    total_q, hq, d = q.shape
+    hkv = k.shape[1]
+    batch = cu_seqlens_q.shape[0] - 1
+    if max_k_tiles is None:
+        max_k_tiles = max(1, (_max_len(cu_seqlens_k) + 127) // 128)
+    if max_seqlen_q is None:
+        max_seqlen_q = 0
+    if output is None:
+        output = torch.empty(((1 if reduce_heads else hq), max_k_tiles, total_q),
+                             dtype=torch.float32, device=q.device)
+    _cuda_contig("output", output, torch.float32)
+    st = L.msa_proxy_score(_p(q), _dtype_code(q), _p(k), _dtype_code(k), _p(cu_seqlens_q),
+                           _p(cu_seqlens_k), None, 0, None, batch, total_q, k.shape[0], hq, hkv, d,
+                           int(max_seqlen_q), int(max_k_tiles), int(bool(causal)),
+                           int(bool(reduce_heads)), _p(output), _stream(stream))
+    _check("msa_proxy_score", st)
+    return output
+
+
+def msa_topk_select(scores, topk, num_kv_heads_out, *, out=None, stream=None):
+    """Top-k block ids per query (ascending, -1 padded); see include/msa.h."""
+    L = lib()
+    _cuda_contig("scores", scores, torch.float32)
+    hs, T, total_q = scores.shape
+    if out is None:
+        out = torch.empty((num_kv_heads_out, total_q, topk), dtype=torch.int32,
+                          device=scores.device)
+    _cuda_contig("out", out, torch.int32)
+    st = L.msa_topk_select(_p(scores), hs, T, total_q, int(topk), int(num_kv_heads_out), _p(out),
+                           _stream(stream))
+    _check("msa_topk_select", st)
+    return out
+
+
+def msa_build_union(q2k_indices, cu_seqlens_q, cu_seqlens_k=None, *, seqused_k=None,
+                    max_pages=0, causal=True, tile_tokens=16, max_tiles=None, stream=None):
+    """Per-tile union metadata in the canonical format; see include/msa.h.
+
+    Returns (union_len, union_blocks, member, tile_info) sized for max_tiles
+    (default ceil(total_q / tile_tokens) + batch).
+    """
+    L = lib()
+    _cuda_contig("q2k_indices", q2k_indices, torch.int32)
+    hkv, total_q, topk = q2k_indices.shape
+    batch = cu_seqlens_q.shape[0] - 1
+    if max_tiles is None:
+        max_tiles = (total_q + tile_tokens - 1) // tile_tokens + batch
+    cap = tile_tokens * topk
+    words = (cap + 31) // 32
+    dev = q2k_indices.device
+    ulen = torch.empty((hkv, max_tiles), dtype=torch.int32, device=dev)
+    ublk = torch.empty((hkv, max_tiles, cap), dtype=torch.int32, device=dev)
+    mem = torch.empty((hkv, max_tiles, tile_tokens, words), dtype=torch.int32, device=dev)
+    info = torch.empty((max_tiles, 2), dtype=torch.int32, device=dev)
+    st = L.msa_build_union(_p(q2k_indices), topk, _p(cu_seqlens_q), _p(cu_seqlens_k),
+                           _p(seqused_k), int(max_pages), batch, total_q, hkv, int(bool(causal)),
+                           int(tile_tokens), int(max_tiles), _p(ulen), _p(ublk), _p(mem),
+                           _p(info), _stream(stream))
+    _check("msa_build_union", st)
+    return ulen, ublk, mem, info
+
+
+def msa_read_device_fault(stream=None) -> int:
+    """Synchronise the stream, return and clear the library's device fault word."""
+    v = C.c_uint(0)
+    _check("msa_read_device_fault", lib().msa_read_device_fault(C.byref(v), _stream(stream)))
+    return int(v.value)
+
+
+def msa_set_timing_events(events=None):
+    """Record three torch.cuda.Event objects around the forward's launches
+    (before, after the metadata step, after attention); None turns it off."""
+    if not events:
+        _check("msa_set_timing_events", lib().msa_set_timing_events(None, 0))
+        return
+    arr = (C.c_void_p * 3)(*[C.c_void_p(e.cuda_event) for e in events])
+    _check("msa_set_timing_events", lib().msa_set_timing_events(arr, 3))

@@ -1,0 +1,438 @@
+// C ABI of libmsa: host-side validation, workspace layout, tensor-map
+// encoding and kernel launches. No allocation, no host synchronisation
+// (except msa_read_device_fault, which exists to synchronise).
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/msa.h"
+#include "internal.h"
+#include "tmap.h"
+
+namespace msa {
+
+__device__ unsigned g_msa_fault_word;
+
+unsigned* fault_word() {
+  static std::mutex mu;
+  static unsigned* addr[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_msa_fault_word) == cudaSuccess) addr[dev] = static_cast<unsigned*>(p);
+  }
+  return addr[dev];
+}
+
+namespace {
+
+constexpr int kMaxTopk = 64;
+constexpr int kDecodeMaxSq = 4;
+constexpr int kDecodeMaxGroup = 16;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int tile_tokens_for(int hq, int hkv) {
+  if (hkv <= 0 || hq <= 0) return 0;
+  const int G = hq / hkv;
+  return G >= 128 ? 1 : 128 / G;
+}
+
+struct PrefillLayout {
+  int W, max_tiles, cap, words;
+  size_t off_info, off_len, off_blocks, off_member, total;
+};
+
+PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk) {
+  PrefillLayout L{};
+  L.W = tile_tokens_for(hq, hkv);
+  L.max_tiles = (total_q + L.W - 1) / L.W + batch;
+  L.cap = L.W * topk;
+  L.words = (L.cap + 31) / 32;
+  size_t off = 0;
+  L.off_info = off;
+  off += up256((size_t)L.max_tiles * 2 * sizeof(int32_t));
+  L.off_len = off;
+  off += up256((size_t)hkv * L.max_tiles * sizeof(int32_t));
+  L.off_blocks = off;
+  off += up256((size_t)hkv * L.max_tiles * L.cap * sizeof(int32_t));
+  L.off_member = off;
+  off += up256((size_t)hkv * L.max_tiles * L.W * L.words * sizeof(uint32_t));
+  L.total = off;
+  return L;
+}
+
+struct DecodeLayout {
+  int rows, pps, splits;
+  size_t off_o, off_ml, off_tickets, total;
+};
+
+DecodeLayout decode_layout(int batch, int hq, int hkv, int topk, int sq_max) {
+  DecodeLayout L{};
+  const int G = hq / hkv;
+  L.rows = G * sq_max;
+  const int R = L.rows <= 16 ? 16 : (L.rows <= 32 ? 32 : 64);
+  L.pps = decode_pages_per_split(L.rows);
+  L.splits = (sq_max * topk + L.pps - 1) / L.pps;
+  const size_t parts = (size_t)batch * hkv * L.splits;
+  size_t off = 0;
+  L.off_o = off;
+  off += up256(parts * R * 128 * sizeof(float));
+  L.off_ml = off;
+  off += up256(parts * R * 2 * sizeof(float));
+  L.off_tickets = off;
+  off += up256((size_t)batch * hkv * sizeof(int));
+  L.total = off;
+  return L;
+}
+
+bool use_decode(bool paged, int max_seqlen_q, int G, msa_dtype_t kv_dtype) {
+  return paged && max_seqlen_q <= kDecodeMaxSq && G <= kDecodeMaxGroup && kv_dtype == MSA_BF16;
+}
+
+// (d, H, T) map over a (T, H, d) tensor; element size 2 (bf16) or 1 (e4m3).
+bool map_rows(CUtensorMap* m, const void* base, int esize, int H, long long T, uint32_t box_h,
+              uint32_t box_t) {
+  const uint64_t dims[3] = {128, (uint64_t)H, (uint64_t)(T > 0 ? T : 1)};
+  const uint64_t strides[2] = {128ull * esize, 128ull * esize * H};
+  const uint32_t box[3] = {esize == 2 ? 64u : 128u, box_h, box_t};  // 128-byte inner box
+  return encode_tiled(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                      3, base, dims, strides, box);
+}
+
+// (d, 128, H, pages) map over a (pages, H, 128, d) paged cache.
+bool map_pages(CUtensorMap* m, const void* base, int esize, int H, int pages) {
+  const uint64_t dims[4] = {128, 128, (uint64_t)H, (uint64_t)pages};
+  const uint64_t strides[3] = {128ull * esize, 128ull * 128 * esize, 128ull * 128 * esize * H};
+  const uint32_t box[4] = {esize == 2 ? 64u : 128u, 128u, 1u, 1u};
+  return encode_tiled(m, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                      4, base, dims, strides, box);
+}
+
+msa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_CUDA_ERROR; }
+
+cudaEvent_t g_timing[3] = {nullptr, nullptr, nullptr};
+bool g_timing_on = false;
+
+void mark(int i, cudaStream_t s) {
+  if (g_timing_on) cudaEventRecord(g_timing[i], s);
+}
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+const char* msa_status_string(msa_status_t s) {
+  switch (s) {
+    case MSA_OK: return "MSA_OK";
+    case MSA_INVALID_ARG: return "MSA_INVALID_ARG";
+    case MSA_UNSUPPORTED: return "MSA_UNSUPPORTED";
+    case MSA_WORKSPACE_TOO_SMALL: return "MSA_WORKSPACE_TOO_SMALL";
+    case MSA_CUDA_ERROR: return "MSA_CUDA_ERROR";
+  }
+  return "MSA_UNKNOWN_STATUS";
+}
+
+int msa_union_tile_tokens(int num_qo_heads, int num_kv_heads) {
+  return tile_tokens_for(num_qo_heads, num_kv_heads);
+}
+
+size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_heads,
+                                           int num_kv_heads, int head_dim, int topk,
+                                           int max_seqlen_q, int paged) {
+  if (batch < 1 || total_q < 0 || num_qo_heads < 1 || num_kv_heads < 1 ||
+      num_qo_heads % num_kv_heads != 0 || head_dim != 128 || topk < 1 || topk > kMaxTopk ||
+      num_qo_heads / num_kv_heads > 128)
+    return 0;
+  size_t bytes = prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk).total;
+  const int G = num_qo_heads / num_kv_heads;
+  if (paged && max_seqlen_q >= 1 && max_seqlen_q <= kDecodeMaxSq && G <= kDecodeMaxGroup) {
+    const size_t d = decode_layout(batch, num_qo_heads, num_kv_heads, topk, max_seqlen_q).total;
+    if (d > bytes) bytes = d;
+  }
+  return bytes;
+}
+
+msa_status_t msa_sparse_attention_fwd(
+    const void* q, msa_dtype_t q_dtype, const void* k, const void* v, msa_dtype_t kv_dtype,
+    const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, const int32_t* page_table, int max_pages, int num_pages,
+    const int32_t* seqused_k, int batch, int total_q, int total_k, int num_qo_heads,
+    int num_kv_heads, int head_dim, int max_seqlen_q, int causal, float softmax_scale, void* out,
+    float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  // ---- argument checks (host only; nothing is read from the device) ----
+  const bool paged = page_table != nullptr;
+  if (cu_seqlens_k != nullptr && paged) return MSA_INVALID_ARG;   // two length sources
+  if (cu_seqlens_k == nullptr && !paged) return MSA_INVALID_ARG;  // no length source
+  if (paged && (seqused_k == nullptr || max_pages < 1 || num_pages < 1)) return MSA_INVALID_ARG;
+  if (!paged && seqused_k != nullptr) return MSA_INVALID_ARG;
+  if (q == nullptr || k == nullptr || v == nullptr || q2k_indices == nullptr ||
+      cu_seqlens_q == nullptr || out == nullptr)
+    return MSA_INVALID_ARG;
+  if (batch < 1 || total_q < 0 || num_qo_heads < 1 || num_kv_heads < 1) return MSA_INVALID_ARG;
+  if (num_qo_heads % num_kv_heads != 0) return MSA_INVALID_ARG;
+  if (!paged && total_k < 1) return MSA_INVALID_ARG;
+  if (total_q > 0 && max_seqlen_q < 1) return MSA_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(q2k_indices, 4) || !aligned(cu_seqlens_q, 4) ||
+      (cu_seqlens_k && !aligned(cu_seqlens_k, 4)) || (page_table && !aligned(page_table, 4)) ||
+      (seqused_k && !aligned(seqused_k, 4)) || (lse && !aligned(lse, 4)) ||
+      (workspace && !aligned(workspace, 256)))
+    return MSA_INVALID_ARG;
+  if (head_dim != 128) return MSA_UNSUPPORTED;
+  if (q_dtype != MSA_BF16) return MSA_UNSUPPORTED;
+  if (kv_dtype != MSA_BF16 && kv_dtype != MSA_FP8_E4M3) return MSA_UNSUPPORTED;
+  if (topk < 1 || topk > kMaxTopk) return MSA_UNSUPPORTED;
+  const int G = num_qo_heads / num_kv_heads;
+  if (G > 128) return MSA_UNSUPPORTED;
+  const size_t need = msa_sparse_attention_workspace_size(
+      batch, total_q, num_qo_heads, num_kv_heads, head_dim, topk, max_seqlen_q, paged ? 1 : 0);
+  if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return MSA_WORKSPACE_TOO_SMALL;
+  if (total_q == 0) return MSA_OK;
+  unsigned* fault = fault_word();
+  if (fault == nullptr) return MSA_CUDA_ERROR;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  const int esize = kv_dtype == MSA_FP8_E4M3 ? 1 : 2;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+  if (use_decode(paged, max_seqlen_q, G, kv_dtype)) {
+    const DecodeLayout L = decode_layout(batch, num_qo_heads, num_kv_heads, topk, max_seqlen_q);
+    DecodeArgs a{};
+    a.fault = fault;
+    if (!map_rows(&a.tmap_q, q, 2, num_qo_heads, total_q, (uint32_t)G, (uint32_t)max_seqlen_q) ||
+        !map_pages(&a.tmap_k, k, 2, num_kv_heads, num_pages) ||
+        !map_pages(&a.tmap_v, v, 2, num_kv_heads, num_pages))
+      return MSA_CUDA_ERROR;
+    a.q2k = q2k_indices;
+    a.topk = topk;
+    a.cu_q = cu_seqlens_q;
+    a.page_table = page_table;
+    a.max_pages = max_pages;
+    a.num_pages = num_pages;
+    a.seqused_k = seqused_k;
+    a.batch = batch;
+    a.total_q = total_q;
+    a.num_qo_heads = num_qo_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.sq_max = max_seqlen_q;
+    a.causal = causal ? 1 : 0;
+    a.scale_log2 = scale_log2;
+    a.out = out;
+    a.lse = lse;
+    a.pages_per_split = L.pps;
+    a.splits = L.splits;
+    a.part_o = reinterpret_cast<float*>(ws + L.off_o);
+    a.part_ml = reinterpret_cast<float*>(ws + L.off_ml);
+    a.tickets = reinterpret_cast<int*>(ws + L.off_tickets);
+    mark(0, stream);
+    cudaError_t e = cudaMemsetAsync(a.tickets, 0, (size_t)batch * num_kv_heads * sizeof(int), stream);
+    if (e != cudaSuccess) return MSA_CUDA_ERROR;
+    mark(1, stream);
+    e = launch_decode(a, stream);
+    mark(2, stream);
+    return from_cuda(e);
+  }
+
+  const PrefillLayout L = prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk);
+  UnionArgs u{};
+  u.q2k = q2k_indices;
+  u.topk = topk;
+  u.cu_q = cu_seqlens_q;
+  u.cu_k = cu_seqlens_k;
+  u.seqused_k = seqused_k;
+  u.max_pages = max_pages;
+  u.batch = batch;
+  u.total_q = total_q;
+  u.num_kv_heads = num_kv_heads;
+  u.causal = causal ? 1 : 0;
+  u.tile_tokens = L.W;
+  u.max_tiles = L.max_tiles;
+  u.cap = L.cap;
+  u.words = L.words;
+  u.union_len = reinterpret_cast<int32_t*>(ws + L.off_len);
+  u.union_blocks = reinterpret_cast<int32_t*>(ws + L.off_blocks);
+  u.member = reinterpret_cast<uint32_t*>(ws + L.off_member);
+  u.tile_info = reinterpret_cast<int32_t*>(ws + L.off_info);
+  mark(0, stream);
+  cudaError_t e = launch_build_union(u, stream);
+  if (e != cudaSuccess) return MSA_CUDA_ERROR;
+  mark(1, stream);
+
+  PrefillArgs a{};
+  a.fault = fault;
+  bool ok = map_rows(&a.tmap_q, q, 2, num_qo_heads, total_q, (uint32_t)G, (uint32_t)L.W);
+  if (paged) {
+    ok = ok && map_pages(&a.tmap_k, k, esize, num_kv_heads, num_pages) &&
+         map_pages(&a.tmap_v, v, esize, num_kv_heads, num_pages);
+  } else {
+    ok = ok && map_rows(&a.tmap_k, k, esize, num_kv_heads, total_k, 1, 128) &&
+         map_rows(&a.tmap_v, v, esize, num_kv_heads, total_k, 1, 128);
+  }
+  if (!ok) return MSA_CUDA_ERROR;
+  a.paged = paged ? 1 : 0;
+  a.kv_fp8 = esize == 1 ? 1 : 0;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.page_table = page_table;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.seqused_k = seqused_k;
+  a.batch = batch;
+  a.total_q = total_q;
+  a.num_qo_heads = num_qo_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale_log2;
+  a.tile_tokens = L.W;
+  a.max_tiles = L.max_tiles;
+  a.cap = L.cap;
+  a.words = L.words;
+  a.union_len = u.union_len;
+  a.union_blocks = u.union_blocks;
+  a.member = u.member;
+  a.tile_info = u.tile_info;
+  a.out = out;
+  a.lse = lse;
+  e = launch_prefill(a, stream);
+  mark(2, stream);
+  return from_cuda(e);
+}
+
+msa_status_t msa_proxy_score(const void* q, msa_dtype_t q_dtype, const void* k,
+                             msa_dtype_t k_dtype, const int32_t* cu_seqlens_q,
+                             const int32_t* cu_seqlens_k, const int32_t* page_table, int max_pages,
+                             const int32_t* seqused_k, int batch, int total_q, int total_k,
+                             int num_qo_heads, int num_kv_heads, int head_dim, int max_seqlen_q,
+                             int max_k_tiles, int causal, int reduce_heads, float* output,
+                             cudaStream_t stream) {
+  (void)max_pages;
+  (void)max_seqlen_q;
+  if (page_table != nullptr || seqused_k != nullptr) {
+    if (cu_seqlens_k != nullptr) return MSA_INVALID_ARG;
+    return MSA_UNSUPPORTED;  // the paged proxy is not built
+  }
+  if (q == nullptr || k == nullptr || cu_seqlens_q == nullptr || cu_seqlens_k == nullptr ||
+      output == nullptr)
+    return MSA_INVALID_ARG;
+  if (batch < 1 || total_q < 0 || total_k < 1 || num_qo_heads < 1 || num_kv_heads < 1 ||
+      num_qo_heads % num_kv_heads != 0 || max_k_tiles < 1)
+    return MSA_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(output, 4) || !aligned(cu_seqlens_q, 4) ||
+      !aligned(cu_seqlens_k, 4))
+    return MSA_INVALID_ARG;
+  if (head_dim != 128 || q_dtype != MSA_BF16 || k_dtype != MSA_BF16) return MSA_UNSUPPORTED;
+  const int G = num_qo_heads / num_kv_heads;
+  if (G > 128) return MSA_UNSUPPORTED;
+  if (reduce_heads && (G > 32 || (G & (G - 1)) != 0)) return MSA_UNSUPPORTED;
+  if (total_q == 0) return MSA_OK;
+  ProxyArgs a{};
+  a.fault = fault_word();
+  if (a.fault == nullptr) return MSA_CUDA_ERROR;
+  const int Wm = tile_tokens_for(num_qo_heads, num_kv_heads);
+  if (!map_rows(&a.tmap_q, q, 2, num_qo_heads, total_q, (uint32_t)G, (uint32_t)Wm) ||
+      !map_rows(&a.tmap_k, k, 2, num_kv_heads, total_k, 1, 128))
+    return MSA_CUDA_ERROR;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.batch = batch;
+  a.total_q = total_q;
+  a.num_qo_heads = num_qo_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.max_k_tiles = max_k_tiles;
+  a.causal = causal ? 1 : 0;
+  a.reduce_heads = reduce_heads ? 1 : 0;
+  a.tile_tokens = Wm;
+  a.max_tiles = (total_q + 2 * Wm - 1) / (2 * Wm) + batch;
+  a.out = output;
+  return from_cuda(launch_proxy(a, stream));
+}
+
+msa_status_t msa_topk_select(const float* scores, int num_score_heads, int max_k_tiles,
+                             int total_q, int topk, int num_kv_heads_out, int32_t* q2k_indices,
+                             cudaStream_t stream) {
+  if (scores == nullptr || q2k_indices == nullptr) return MSA_INVALID_ARG;
+  if (num_score_heads < 1 || max_k_tiles < 1 || total_q < 0 || num_kv_heads_out < 1)
+    return MSA_INVALID_ARG;
+  if (num_score_heads != 1 && num_score_heads != num_kv_heads_out) return MSA_INVALID_ARG;
+  if (!aligned(scores, 4) || !aligned(q2k_indices, 4)) return MSA_INVALID_ARG;
+  if (topk < 1 || topk > kMaxTopk) return MSA_UNSUPPORTED;
+  if (total_q == 0) return MSA_OK;
+  TopkArgs a{scores, num_score_heads, max_k_tiles, total_q, topk, num_kv_heads_out, q2k_indices};
+  return from_cuda(launch_topk(a, stream));
+}
+
+msa_status_t msa_build_union(const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+                             const int32_t* cu_seqlens_k, const int32_t* seqused_k, int max_pages,
+                             int batch, int total_q, int num_kv_heads, int causal, int tile_tokens,
+                             int max_tiles, int32_t* union_len, int32_t* union_blocks,
+                             uint32_t* member, int32_t* tile_info, cudaStream_t stream) {
+  if (q2k_indices == nullptr || cu_seqlens_q == nullptr || union_len == nullptr ||
+      union_blocks == nullptr || member == nullptr)
+    return MSA_INVALID_ARG;
+  if ((cu_seqlens_k == nullptr) == (seqused_k == nullptr)) return MSA_INVALID_ARG;
+  if (seqused_k != nullptr && max_pages < 1) return MSA_INVALID_ARG;
+  if (batch < 1 || total_q < 0 || num_kv_heads < 1 || max_tiles < 0) return MSA_INVALID_ARG;
+  if (tile_tokens < 1 || tile_tokens > 128) return MSA_INVALID_ARG;
+  if (topk < 1 || topk > kMaxTopk) return MSA_UNSUPPORTED;
+  if (max_tiles == 0) return MSA_OK;
+  UnionArgs u{};
+  u.q2k = q2k_indices;
+  u.topk = topk;
+  u.cu_q = cu_seqlens_q;
+  u.cu_k = cu_seqlens_k;
+  u.seqused_k = seqused_k;
+  u.max_pages = max_pages;
+  u.batch = batch;
+  u.total_q = total_q;
+  u.num_kv_heads = num_kv_heads;
+  u.causal = causal ? 1 : 0;
+  u.tile_tokens = tile_tokens;
+  u.max_tiles = max_tiles;
+  u.cap = tile_tokens * topk;
+  u.words = (u.cap + 31) / 32;
+  u.union_len = union_len;
+  u.union_blocks = union_blocks;
+  u.member = member;
+  u.tile_info = tile_info;
+  return from_cuda(launch_build_union(u, stream));
+}
+
+msa_status_t msa_set_timing_events(void* const* events, int count) {
+  if (count == 0) {
+    g_timing_on = false;
+    return MSA_OK;
+  }
+  if (count != 3 || events == nullptr) return MSA_INVALID_ARG;
+  for (int i = 0; i < 3; ++i) {
+    if (events[i] == nullptr) return MSA_INVALID_ARG;
+    g_timing[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  g_timing_on = true;
+  return MSA_OK;
+}
+
+msa_status_t msa_read_device_fault(unsigned int* fault, cudaStream_t stream) {
+  if (fault == nullptr) return MSA_INVALID_ARG;
+  unsigned* dev = fault_word();
+  if (dev == nullptr) return MSA_CUDA_ERROR;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MSA_CUDA_ERROR;
+  unsigned host = 0;
+  if (cudaMemcpy(&host, dev, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MSA_CUDA_ERROR;
+  const unsigned zero = 0;
+  if (cudaMemcpy(dev, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return MSA_CUDA_ERROR;
+  *fault = host;
+  return MSA_OK;
+}
+
+}  // extern "C"

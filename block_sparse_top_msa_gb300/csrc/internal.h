@@ -1,0 +1,130 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+// Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace msa {
+
+// Device address of the library's fault word on the current device (host).
+unsigned* fault_word();
+
+struct UnionArgs {
+  const int32_t* q2k;
+  int topk;
+  const int32_t* cu_q;
+  const int32_t* cu_k;       // flat lengths, or NULL
+  const int32_t* seqused_k;  // paged lengths, or NULL
+  int max_pages;
+  int batch;
+  int total_q;
+  int num_kv_heads;
+  int causal;
+  int tile_tokens;  // W
+  int max_tiles;
+  int cap;          // W * topk
+  int words;        // ceil(cap / 32)
+  int32_t* union_len;
+  int32_t* union_blocks;
+  uint32_t* member;
+  int32_t* tile_info;  // may be NULL
+};
+cudaError_t launch_build_union(const UnionArgs& a, cudaStream_t s);
+
+struct TopkArgs {
+  const float* scores;
+  int num_score_heads;
+  int max_k_tiles;
+  int total_q;
+  int topk;
+  int num_kv_heads_out;
+  int32_t* q2k;
+};
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
+
+struct DecodeArgs {
+  unsigned* fault;      // device fault word (bounded-wait expiry, capacity)
+  CUtensorMap tmap_q;   // (d, Hq, Tq) bf16, box (64, G, sq_max)
+  CUtensorMap tmap_k;   // (d, 128, Hkv, pages) bf16, box (64, 128, 1, 1)
+  CUtensorMap tmap_v;
+  const int32_t* q2k;
+  int topk;
+  const int32_t* cu_q;
+  const int32_t* page_table;
+  int max_pages;
+  int num_pages;
+  const int32_t* seqused_k;
+  int batch;
+  int total_q;
+  int num_qo_heads;
+  int num_kv_heads;
+  int sq_max;           // max_seqlen_q (<= 4)
+  int causal;
+  float scale_log2;     // softmax_scale * log2(e)
+  void* out;
+  float* lse;
+  int pages_per_split;
+  int splits;           // per (request, kv head)
+  float* part_o;        // (B*Hkv*splits, rows_max, 128)
+  float* part_ml;       // (B*Hkv*splits, rows_max, 2)
+  int* tickets;         // (B*Hkv)
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+size_t decode_workspace_bytes(int batch, int num_kv_heads, int rows_max, int splits);
+int decode_pages_per_split(int rows);
+
+struct PrefillArgs {
+  unsigned* fault;      // device fault word (bounded-wait expiry, capacity)
+  CUtensorMap tmap_q;   // (d, Hq, Tq) bf16, box (64, G, W)
+  CUtensorMap tmap_k;   // flat (d or d bytes, Hkv, Tk) / paged (.., 128, Hkv, pages)
+  CUtensorMap tmap_v;
+  int paged;
+  int kv_fp8;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* page_table;
+  int max_pages;
+  int num_pages;
+  const int32_t* seqused_k;
+  int batch;
+  int total_q;
+  int num_qo_heads;
+  int num_kv_heads;
+  int causal;
+  float scale_log2;
+  int tile_tokens;
+  int max_tiles;
+  int cap;
+  int words;
+  const int32_t* union_len;
+  const int32_t* union_blocks;
+  const uint32_t* member;
+  const int32_t* tile_info;
+  void* out;
+  float* lse;
+};
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+
+struct ProxyArgs {
+  unsigned* fault;      // device fault word (bounded-wait expiry, capacity)
+  CUtensorMap tmap_q;   // (d, Hq, Tq) bf16, box (64, G, Wm)
+  CUtensorMap tmap_k;   // (d, Hkv, Tk) bf16, box (64, 1, 128)
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int batch;
+  int total_q;
+  int num_qo_heads;
+  int num_kv_heads;
+  int max_k_tiles;
+  int causal;
+  int reduce_heads;
+  int tile_tokens;      // tokens per M-tile (128 / G)
+  int max_tiles;        // upper bound on query tiles of 2 M-tiles each
+  float* out;
+};
+cudaError_t launch_proxy(const ProxyArgs& a, cudaStream_t s);
+
+}  // namespace msa

@@ -1,0 +1,200 @@
+/*
+ * libmsa — MiniMax Sparse Attention (MSA) forward for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI. Every pointer argument marked "device" is a CUDA device pointer the
+ * caller allocated and owns; the library allocates no memory, never
+ * synchronises the host with the device, and enqueues all work on the
+ * caller's stream. All tensors are dense and contiguous (row-major, last
+ * dimension fastest) in the layouts stated below, which are those of the
+ * FlashInfer MSA documentation pages ("flashinfer.msa_ops.msa_sparse_attention",
+ * "flashinfer.msa_ops.msa_proxy_score", "prepare_msa_nvfp4_sparse_decode").
+ *
+ * Errors: every entry point validates its arguments on the host before any
+ * launch and returns a status. Index values and cu_seqlens contents are caller
+ * contracts and are never copied back to the host; kernels mask out-of-range
+ * block ids and page ids instead of faulting. Device pointers must be 16-byte
+ * aligned.
+ *
+ * Sizes used below: Tq = total_q, Tk = total_k, Hq = num_qo_heads,
+ * Hkv = num_kv_heads, G = Hq / Hkv, d = head_dim (128), B = batch,
+ * BLK = 128 (KV block = page size in tokens).
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MSA_OK = 0,
+  MSA_INVALID_ARG = 1,          /* malformed or conflicting arguments */
+  MSA_UNSUPPORTED = 2,          /* valid but outside this build (dtype, head_dim, sizes) */
+  MSA_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the size query's answer */
+  MSA_CUDA_ERROR = 4            /* a CUDA runtime/driver call failed at launch */
+} msa_status_t;
+
+typedef enum { MSA_BF16 = 0, MSA_FP16 = 1, MSA_FP8_E4M3 = 2 } msa_dtype_t;
+
+/* Human-readable name of a status code (static storage). */
+const char* msa_status_string(msa_status_t status);
+
+/*
+ * Workspace bytes msa_sparse_attention_fwd needs for these sizes
+ * ("msa_sparse_attention", workspace: caller-owned storage). paged != 0 when
+ * K/V come with a page table. Returns 0 for sizes the forward would reject.
+ */
+size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_heads,
+                                           int num_kv_heads, int head_dim, int topk,
+                                           int max_seqlen_q, int paged);
+
+/*
+ * Sparse attention forward ("flashinfer.msa_ops.msa_sparse_attention").
+ *
+ * Each query token t and query head h attends only to the keys of the 128-token
+ * KV blocks listed in q2k_indices[h / G, t, :] (batch-local block ids,
+ * ascending, -1 padded), with right-aligned causal masking when causal != 0
+ * (query i of a sequence with Lq queries and Lk keys sits at key position
+ * Lk - Lq + i) and query head h reading KV head h / G (GQA; "prepare_msa_nvfp4_
+ * sparse_decode", q). The result equals per-query softmax attention over that
+ * query's own blocks: out = softmax(scale * q k^T) v over the selected visible
+ * keys; lse = natural log of the softmax normaliser. A row with no visible
+ * selected key gets out = 0 and lse = -inf. Query tokens are processed in
+ * tiles that each run one online softmax over the union of their tokens'
+ * blocks; the union metadata is built into the workspace.
+ *
+ *   q            device, (Tq, Hq, d), q_dtype (MSA_BF16)
+ *   k, v         device; flat (Tk, Hkv, d) when page_table == NULL, else
+ *                paged (num_pages, Hkv, BLK, d); kv_dtype MSA_BF16 or MSA_FP8_E4M3
+ *                (E4M3 "fn", upconverted exactly in-kernel; needs bf16 q)
+ *   q2k_indices  device int32 (Hkv, Tq, topk); 1 <= topk <= 64
+ *   cu_seqlens_q device int32 (B+1), cumulative query lengths
+ *   cu_seqlens_k device int32 (B+1) for flat K/V; must be NULL when paged
+ *   page_table   device int32 (B, max_pages) mapping batch-local block -> page,
+ *                or NULL for flat K/V; requires seqused_k
+ *   seqused_k    device int32 (B), valid keys per sequence (paged only)
+ *   max_seqlen_q host bound on every Lq; the paged route with max_seqlen_q <= 4
+ *                and G <= 16 runs the split-KV decode kernel
+ *   softmax_scale  <= 0 selects head_dim^-0.5
+ *   out          device, (Tq, Hq, d), dtype of q; fully written
+ *   lse          device float32 (Tq, Hq) or NULL
+ *   workspace    device scratch of at least
+ *                msa_sparse_attention_workspace_size(...) bytes, 256-byte
+ *                aligned; its contents need no initialisation, and calls that
+ *                share one workspace must be ordered on the device.
+ * Returns MSA_INVALID_ARG when both or neither of cu_seqlens_k and page_table
+ * are given (paged length comes only from seqused_k, per the page's rule of
+ * declining two possibly disagreeing length sources), when Hq % Hkv != 0, or
+ * when a pointer is NULL or misaligned; MSA_UNSUPPORTED for head_dim != 128,
+ * q not bf16, or topk outside [1, 64].
+ */
+msa_status_t msa_sparse_attention_fwd(
+    const void* q, msa_dtype_t q_dtype, const void* k, const void* v, msa_dtype_t kv_dtype,
+    const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, const int32_t* page_table, int max_pages, int num_pages,
+    const int32_t* seqused_k, int batch, int total_q, int total_k, int num_qo_heads,
+    int num_kv_heads, int head_dim, int max_seqlen_q, int causal, float softmax_scale, void* out,
+    float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Dense proxy pass, MSA stage 1 ("flashinfer.msa_ops.msa_proxy_score").
+ *
+ * output[h, t, q] = max over the keys j of KV block t of the UNSCALED logit
+ * <q[q, h, :], k[j, h / G, :]>, with j < Lk and, when causal, j <= Lk - Lq + i
+ * (right-aligned, applied before the max); -inf when block t holds no such key
+ * (beyond the sequence or wholly above the causal limit). With
+ * reduce_heads != 0 the max is also taken over all query heads and the output
+ * has one head.
+ *
+ *   q            device, (Tq, Hq, 128), MSA_BF16
+ *   k            device, flat (Tk, Hkv, 128), MSA_BF16
+ *   cu_seqlens_q, cu_seqlens_k  device int32 (B+1)
+ *   page_table, seqused_k       must be NULL (the paged proxy is not built)
+ *   max_k_tiles  number of block columns; blocks >= ceil(Lk/128) read -inf
+ *   output       device float32 (reduce_heads ? 1 : Hq, max_k_tiles, Tq),
+ *                query fastest; fully written
+ */
+msa_status_t msa_proxy_score(const void* q, msa_dtype_t q_dtype, const void* k,
+                             msa_dtype_t k_dtype, const int32_t* cu_seqlens_q,
+                             const int32_t* cu_seqlens_k, const int32_t* page_table, int max_pages,
+                             const int32_t* seqused_k, int batch, int total_q, int total_k,
+                             int num_qo_heads, int num_kv_heads, int head_dim, int max_seqlen_q,
+                             int max_k_tiles, int causal, int reduce_heads, float* output,
+                             cudaStream_t stream);
+
+/*
+ * Top-k block selection from proxy scores (the consumer named by
+ * "msa_proxy_score", Returns; output contract of q2k_indices in
+ * "msa_sparse_attention" and "prepare_msa_nvfp4_sparse_decode").
+ *
+ * For each query q, the topk largest scores among its max_k_tiles columns;
+ * equal scores go to the lower block id; -inf and NaN are never chosen. The
+ * chosen ids are written ascending and -1 padded.
+ *
+ *   scores       device float32 (num_score_heads, max_k_tiles, Tq)
+ *   num_score_heads  1 (broadcast to all num_kv_heads_out heads) or
+ *                num_kv_heads_out (one selection per head)
+ *   q2k_indices  device int32 (num_kv_heads_out, Tq, topk); 1 <= topk <= 64
+ */
+msa_status_t msa_topk_select(const float* scores, int num_score_heads, int max_k_tiles,
+                             int total_q, int topk, int num_kv_heads_out, int32_t* q2k_indices,
+                             cudaStream_t stream);
+
+/*
+ * Query-tile union metadata ("msa_sparse_attention": "the union metadata is
+ * built internally from q2k_indices"), exported so it can be checked on its
+ * own. Tiles are tile_tokens consecutive queries of one sequence, numbered in
+ * sequence order; tile tau of KV head h:
+ *   union_len[h, tau]              number of distinct usable ids
+ *   union_blocks[h, tau, 0:cap]    those ids ascending, -1 filled
+ *   member[h, tau, w, 0:words]     bit j set iff union_blocks[h, tau, j] is in
+ *                                  the row of the tile's token w
+ *   tile_info[tau, 0:2]            (first packed query row, sequence), or
+ *                                  (-1, -1) past the last tile; may be NULL
+ * with cap = tile_tokens * topk and words = ceil(cap / 32). An id is usable for
+ * a token iff 0 <= id < ceil(Lk/128) (and id < max_pages when paged) and, when
+ * causal, its block holds a key at or before the token's position. Rows past a
+ * sequence end are zero. Arrays are sized for max_tiles tiles, which must be
+ * at least the number of tiles, sum_b ceil(Lq_b / tile_tokens); tiles past
+ * the last get length 0.
+ *   cu_seqlens_k (flat) or seqused_k (paged): exactly one is non-NULL.
+ * tile_tokens must lie in [1, 128].
+ */
+msa_status_t msa_build_union(const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+                             const int32_t* cu_seqlens_k, const int32_t* seqused_k, int max_pages,
+                             int batch, int total_q, int num_kv_heads, int causal, int tile_tokens,
+                             int max_tiles, int32_t* union_len, int32_t* union_blocks,
+                             uint32_t* member, int32_t* tile_info, cudaStream_t stream);
+
+/* Tokens per query tile the forward uses for Hq/Hkv: floor(128 / G), at least 1. */
+int msa_union_tile_tokens(int num_qo_heads, int num_kv_heads);
+
+/*
+ * Waits for `stream`, then returns and clears the library's device fault word
+ * of the current device in *fault (0 = none). Kernels never trap: a wait that
+ * exceeds its time limit, or an internal capacity check, sets a bit here and
+ * the kernel returns early. Synchronises the host: for tests and diagnostics.
+ */
+msa_status_t msa_read_device_fault(unsigned int* fault, cudaStream_t stream);
+
+/*
+ * Diagnostics: timing events for msa_sparse_attention_fwd. When `events`
+ * points to three cudaEvent_t handles (count == 3), every later forward call
+ * records events[0] before its first launch, events[1] after the metadata
+ * step (union kernel, or the decode ticket reset) and events[2] after the
+ * attention kernel, all on the call's stream. count == 0 turns it off. The
+ * handles are owned by the caller and must outlive their use. Not
+ * thread-safe; meant for benchmarks.
+ */
+msa_status_t msa_set_timing_events(void* const* events, int count);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* MSA_H_ */

@@ -1,0 +1,145 @@
+"""The C-ABI library loads, exports every symbol include/msa.h declares, and
+decides argument errors on the host before touching the GPU (CPU only: every
+call here returns before its first CUDA runtime call)."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "msa.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import block_sparse_top_msa_gb300 as msa
+    msa.build()
+    return msa.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(msa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for f in ("msa_sparse_attention_fwd", "msa_sparse_attention_workspace_size",
+              "msa_proxy_score", "msa_topk_select", "msa_build_union", "msa_status_string",
+              "msa_union_tile_tokens", "msa_read_device_fault"):
+        assert f in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    import block_sparse_top_msa_gb300 as msa
+    out = subprocess.run(["nm", "-D", "--defined-only", msa.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    missing = [f for f in declared_functions() if f not in exported]
+    assert not missing, missing
+    for f in declared_functions():
+        assert hasattr(L, f)
+
+
+def test_status_strings(L):
+    import block_sparse_top_msa_gb300 as msa
+    assert msa.status_string(0) == "MSA_OK"
+    assert msa.status_string(1) == "MSA_INVALID_ARG"
+    assert msa.status_string(2) == "MSA_UNSUPPORTED"
+    assert msa.status_string(3) == "MSA_WORKSPACE_TOO_SMALL"
+    assert msa.status_string(4) == "MSA_CUDA_ERROR"
+    assert msa.status_string(99) == "MSA_UNKNOWN_STATUS"
+
+
+def test_tile_tokens_and_workspace_size(L):
+    import block_sparse_top_msa_gb300 as msa
+    assert msa.msa_union_tile_tokens(64, 8) == 16
+    assert msa.msa_union_tile_tokens(4, 1) == 32
+    assert msa.msa_union_tile_tokens(32, 32) == 128
+    assert msa.msa_union_tile_tokens(256, 1) == 1
+    assert msa.msa_union_tile_tokens(24, 2) == 10  # G = 12: floor(128 / 12)
+    ws = msa.msa_sparse_attention_workspace_size(2, 65536, 64, 8, 128, 16, 32768, 0)
+    # tile info + lengths + union lists + membership words, each 256-byte padded
+    tiles = 65536 // 16 + 2
+    assert ws >= tiles * 8 + 8 * tiles * 4 + 8 * tiles * 256 * 4 + 8 * tiles * 16 * 8 * 4
+    assert msa.msa_sparse_attention_workspace_size(2, 100, 64, 8, 64, 16, 50, 0) == 0
+    assert msa.msa_sparse_attention_workspace_size(2, 100, 64, 7, 128, 16, 50, 0) == 0
+    assert msa.msa_sparse_attention_workspace_size(2, 100, 64, 8, 128, 65, 50, 0) == 0
+    paged = msa.msa_sparse_attention_workspace_size(128, 512, 64, 4, 128, 16, 4, 1)
+    flat = msa.msa_sparse_attention_workspace_size(128, 512, 64, 4, 128, 16, 4, 0)
+    assert paged >= flat > 0
+
+
+A = 0x10000  # a 64 KiB-aligned fake device address; never dereferenced on these paths
+
+
+def fwd(L, **kw):
+    args = dict(q=A, qdt=0, k=A, v=A, kvdt=0, q2k=A, topk=16, cu_q=A, cu_k=A, pt=None,
+                max_pages=0, num_pages=0, su=None, batch=1, total_q=128, total_k=128, hq=8, hkv=2,
+                d=128, max_sq=128, causal=1, scale=0.0, out=A, lse=None, ws=A, ws_bytes=1 << 40,
+                stream=None)
+    args.update(kw)
+    vp = lambda x: None if x is None else C.c_void_p(x)
+    return L.msa_sparse_attention_fwd(
+        vp(args["q"]), args["qdt"], vp(args["k"]), vp(args["v"]), args["kvdt"], vp(args["q2k"]),
+        args["topk"], vp(args["cu_q"]), vp(args["cu_k"]), vp(args["pt"]), args["max_pages"],
+        args["num_pages"], vp(args["su"]), args["batch"], args["total_q"], args["total_k"],
+        args["hq"], args["hkv"], args["d"], args["max_sq"], args["causal"], args["scale"],
+        vp(args["out"]), vp(args["lse"]), vp(args["ws"]), args["ws_bytes"], vp(args["stream"]))
+
+
+def test_forward_argument_errors(L):
+    # Two length sources (cu_seqlens_k and page_table): declined, not resolved.
+    assert fwd(L, pt=A, su=A, max_pages=4, num_pages=4) == 1
+    # No length source at all.
+    assert fwd(L, cu_k=None) == 1
+    # Paged without seqused_k.
+    assert fwd(L, cu_k=None, pt=A, max_pages=4, num_pages=4) == 1
+    assert fwd(L, hq=8, hkv=3) == 1                 # Hq % Hkv != 0
+    assert fwd(L, q=A + 8) == 1                      # misaligned q
+    assert fwd(L, ws=A + 64) == 1                    # misaligned workspace
+    assert fwd(L, q=None) == 1
+    assert fwd(L, total_k=0) == 1
+    assert fwd(L, d=64) == 2                         # head_dim
+    assert fwd(L, qdt=2) == 2                        # fp8 q
+    assert fwd(L, qdt=1) == 2                        # fp16 q: not built
+    assert fwd(L, topk=0) == 2 and fwd(L, topk=65) == 2
+    assert fwd(L, hq=256, hkv=1) == 2                # G > 128
+    assert fwd(L, ws_bytes=16) == 3                  # workspace too small
+    assert fwd(L, total_q=0) == 0                    # nothing to do, no launch
+
+
+def test_other_entry_point_errors(L):
+    vp = C.c_void_p
+    # proxy: paged form is not built; both length kinds -> invalid
+    assert L.msa_proxy_score(vp(A), 0, vp(A), 0, vp(A), None, vp(A), 4, vp(A), 1, 128, 128, 8, 2,
+                             128, 128, 1, 1, 1, vp(A), None) == 2
+    assert L.msa_proxy_score(vp(A), 0, vp(A), 0, vp(A), vp(A), vp(A), 4, vp(A), 1, 128, 128, 8, 2,
+                             128, 128, 1, 1, 1, vp(A), None) == 1
+    assert L.msa_proxy_score(vp(A), 0, vp(A), 0, vp(A), vp(A), None, 0, None, 1, 128, 128, 8, 2,
+                             64, 128, 1, 1, 1, vp(A), None) == 2   # head_dim
+    assert L.msa_proxy_score(vp(A), 0, vp(A), 0, vp(A), vp(A), None, 0, None, 1, 128, 128, 48, 1,
+                             128, 128, 1, 1, 1, vp(A), None) == 2  # reduce_heads, G = 48
+    assert L.msa_proxy_score(vp(A), 0, vp(A), 0, vp(A), vp(A), None, 0, None, 1, 128, 128, 8, 2,
+                             128, 128, 0, 1, 1, vp(A), None) == 1  # max_k_tiles 0
+    # top-k
+    assert L.msa_topk_select(vp(A), 3, 8, 16, 4, 2, vp(A), None) == 1   # heads 3 vs 2
+    assert L.msa_topk_select(vp(A), 1, 8, 16, 65, 2, vp(A), None) == 2  # topk
+    assert L.msa_topk_select(vp(A), 1, 8, 0, 4, 2, vp(A), None) == 0    # empty
+    # union: exactly one length source
+    assert L.msa_build_union(vp(A), 4, vp(A), vp(A), vp(A), 4, 1, 16, 1, 1, 16, 2, vp(A), vp(A),
+                             vp(A), None, None) == 1
+    assert L.msa_build_union(vp(A), 4, vp(A), vp(A), None, 0, 1, 16, 1, 1, 0, 2, vp(A), vp(A),
+                             vp(A), None, None) == 1                     # tile_tokens 0
+    assert L.msa_read_device_fault(None, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import block_sparse_top_msa_gb300 as msa
+    monkeypatch.setattr(msa, "_lib", None)
+    monkeypatch.setattr(msa, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        msa.lib()

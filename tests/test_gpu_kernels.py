@@ -1,0 +1,303 @@
+"""GPU parity of every kernel against the fp64 oracle on small seeded inputs.
+
+Sizes are chosen so the oracle runs in seconds while every case spans several
+query tiles and KV blocks with ragged tails. All calls go through the C ABI
+(via the thin binding).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity_util import check_attention, check_proxy, f32, fault_clear, to_dev
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def msa():
+    import block_sparse_top_msa_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+def _prefill_inputs(lens_q, lens_k, hq, hkv, topk, seed, kv="bf16", first_prev=False):
+    g = torch.Generator().manual_seed(seed)
+    d = 128
+    tq, tk = sum(lens_q), sum(lens_k)
+    q = torch.randn(tq, hq, d, generator=g).to(torch.bfloat16)
+    if kv == "e4m3":
+        k = torch.randn(tk, hkv, d, generator=g).to(torch.float8_e4m3fn)
+        v = torch.randn(tk, hkv, d, generator=g).to(torch.float8_e4m3fn)
+    else:
+        k = torch.randn(tk, hkv, d, generator=g).to(torch.bfloat16)
+        v = torch.randn(tk, hkv, d, generator=g).to(torch.bfloat16)
+    cu_q = workloads.cu_from_lengths(lens_q)
+    cu_k = workloads.cu_from_lengths(lens_k)
+    pos = workloads.query_positions(cu_q, lens_k)
+    q2k = workloads.select_blocks(pos, hkv, topk, g, first=first_prev, prev=first_prev)
+    return dict(q=q, k=k, v=v, q2k_indices=q2k, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k)
+
+
+def _run_prefill(msa, inp, causal=True, scale=None, max_seqlen_q=None):
+    g = to_dev(inp, DEV)
+    out, lse = msa.msa_sparse_attention_fwd(
+        g["q"], g["k"], g["v"], g["q2k_indices"], g["cu_seqlens_q"], g.get("cu_seqlens_k"),
+        causal=causal, softmax_scale=scale, page_table=g.get("page_table"),
+        seqused_k=g.get("seqused_k"), max_seqlen_q=max_seqlen_q, return_softmax_lse=True)
+    torch.cuda.synchronize()
+    fault_clear(msa)
+    return out, lse
+
+
+def _oracle(inp, causal=True, scale=None, rows=None):
+    s = f32(scale if scale is not None else 128 ** -0.5)
+    return oracle.sparse_attention(inp["q"], inp["k"], inp["v"], inp["q2k_indices"],
+                                   inp["cu_seqlens_q"], inp.get("cu_seqlens_k"), causal=causal,
+                                   softmax_scale=s, page_table=inp.get("page_table"),
+                                   seqused_k=inp.get("seqused_k"), rows=rows)
+
+
+# ---------------------------------------------------------------- union metadata
+@pytest.mark.parametrize("W,topk,lens", [(16, 16, [300, 45, 1000]), (32, 4, [1024]),
+                                         (1, 3, [77, 300]), (128, 8, [600, 129]),
+                                         (10, 5, [333])])
+def test_union_bit_exact(msa, W, topk, lens):
+    g = torch.Generator().manual_seed(W * 7 + topk)
+    hkv = 3
+    cu = workloads.cu_from_lengths(lens)
+    pos = workloads.query_positions(cu, lens)
+    q2k = workloads.select_blocks(pos, hkv, topk, g, first=True, prev=True)
+    q2k[0, 5, 0] = 1000          # beyond the sequence
+    q2k[1, 7, -1] = q2k[1, 7, 0]  # duplicate
+    q2k[2, 9, :] = -1             # empty row
+    ref_len, ref_blk, ref_mem = oracle.build_union(q2k, cu, cu, causal=True, tile_tokens=W)
+    T = ref_len.shape[1]
+    ulen, ublk, mem, info = msa.msa_build_union(q2k.to(DEV), cu.to(DEV), cu.to(DEV), causal=True,
+                                                tile_tokens=W)
+    torch.cuda.synchronize()
+    assert np.array_equal(ulen[:, :T].cpu().numpy(), ref_len)
+    assert np.array_equal(ublk[:, :T].cpu().numpy(), ref_blk)
+    assert np.array_equal(mem[:, :T].cpu().numpy().view(np.uint32), ref_mem)
+    assert np.all(ulen[:, T:].cpu().numpy() == 0)
+    infos = info.cpu().numpy()
+    assert np.all(infos[T:] == -1)
+    starts = [s for b, L in enumerate(lens) for s in range(int(cu[b]), int(cu[b]) + L, W)]
+    assert infos[:T, 0].tolist() == starts
+
+
+def test_union_paged_lengths(msa):
+    g = torch.Generator().manual_seed(3)
+    lens_q, seqused = [3, 200], [900, 260]
+    cu = workloads.cu_from_lengths(lens_q)
+    pos = workloads.query_positions(cu, seqused)
+    q2k = workloads.select_blocks(pos, 2, 6, g)
+    su = torch.tensor(seqused, dtype=torch.int32)
+    ref = oracle.build_union(q2k, cu, seqused_k=su, max_pages=5, causal=True, tile_tokens=16)
+    got = msa.msa_build_union(q2k.to(DEV), cu.to(DEV), seqused_k=su.to(DEV), max_pages=5,
+                              causal=True, tile_tokens=16)
+    T = ref[0].shape[1]
+    for r, x in zip(ref, got[:3]):
+        assert np.array_equal(x[:, :T].cpu().numpy().view(r.dtype), r)
+
+
+# ---------------------------------------------------------------- top-k
+@pytest.mark.parametrize("topk,hs,hkv", [(16, 1, 4), (1, 1, 2), (5, 3, 3), (33, 1, 1), (64, 2, 2)])
+def test_topk_bit_exact(msa, topk, hs, hkv):
+    rng = np.random.default_rng(topk + hs)
+    T, n = 97, 1000
+    s = rng.integers(-20, 20, size=(hs, T, n)).astype(np.float32) / 4  # many ties
+    s[rng.random(s.shape) < 0.1] = -np.inf
+    s[rng.random(s.shape) < 0.02] = np.nan
+    s[:, :, 0] = -np.inf  # a query with nothing selectable
+    s[:, 5:, 1] = -np.inf  # fewer than topk selectable
+    ref = oracle.topk_select(s, topk, hkv)
+    got = msa.msa_topk_select(torch.from_numpy(s).to(DEV), topk, hkv)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), ref)
+
+
+# ---------------------------------------------------------------- prefill attention
+PREFILL_CASES = [
+    # name, lens_q, lens_k, hq, hkv, topk, kv, first_prev
+    ("gqa4_varlen_ragged", [300, 129, 517], [300, 129, 517], 8, 2, 5, "bf16", True),
+    ("gqa8_lq_lt_lk", [64, 200, 1], [700, 333, 129], 16, 2, 6, "bf16", False),
+    ("gqa16", [400], [400], 16, 1, 4, "bf16", True),
+    ("mha", [260, 300], [260, 300], 2, 2, 3, "bf16", False),
+    ("gqa2_w64", [500], [500], 4, 2, 4, "bf16", False),
+    ("gqa3_padded_rows", [270, 90], [270, 90], 6, 2, 4, "bf16", False),
+    ("group128_w1", [40], [300], 128, 1, 2, "bf16", False),
+    ("e4m3_gqa4", [300, 517], [300, 517], 8, 2, 5, "e4m3", True),
+    ("e4m3_mha_lq_lt_lk", [100], [900], 2, 2, 7, "e4m3", False),
+    ("topk1", [300], [300], 8, 1, 1, "bf16", False),
+    ("topk64", [1200], [1200], 8, 1, 64, "bf16", False),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES, ids=[c[0] for c in PREFILL_CASES])
+def test_prefill_parity(msa, case):
+    name, lq, lk, hq, hkv, topk, kv, fp = case
+    inp = _prefill_inputs(lq, lk, hq, hkv, topk, seed=len(name), kv=kv, first_prev=fp)
+    out, lse = _run_prefill(msa, inp)
+    ref_out, ref_lse = _oracle(inp)
+    check_attention(out, lse, ref_out, ref_lse, label=name)
+
+
+def test_prefill_non_causal_and_scale(msa):
+    inp = _prefill_inputs([200, 300], [200, 300], 8, 2, 4, seed=9)
+    out, lse = _run_prefill(msa, inp, causal=False, scale=0.05)
+    ref_out, ref_lse = _oracle(inp, causal=False, scale=0.05)
+    check_attention(out, lse, ref_out, ref_lse, label="non_causal")
+
+
+def test_prefill_edge_selections(msa):
+    """Empty rows, duplicates, out-of-range ids, ids above the causal limit,
+    -1 not at the tail, and an empty sequence in the batch."""
+    inp = _prefill_inputs([300, 0, 257], [300, 0, 257], 8, 2, 4, seed=4)
+    q2k = inp["q2k_indices"]
+    q2k[0, 0:20, :] = -1                        # empty rows
+    q2k[1, 30, :] = torch.tensor([1, 1, 1, 1])  # duplicates of a block above the limit
+    q2k[0, 200, :] = torch.tensor([0, -1, 2, 77])
+    q2k[1, 299, :] = torch.tensor([2, 1, 0, 0])  # descending, with a duplicate
+    q2k[0, 310, :] = torch.tensor([5, 6, 7, 8])  # all beyond the sequence
+    out, lse = _run_prefill(msa, inp)
+    ref_out, ref_lse = _oracle(inp)
+    assert np.isneginf(ref_lse[0:20, :4]).all()  # KV head 0 serves query heads 0-3
+    check_attention(out, lse, ref_out, ref_lse, label="edges")
+
+
+def _paged(inp_flat, lens_k, extra_pages=5, seed=0, bad_page=False):
+    """Scatter flat K/V into a permuted page pool (tails filled with other values)."""
+    g = torch.Generator().manual_seed(seed)
+    k, v = inp_flat["k"], inp_flat["v"]
+    hkv, d = k.shape[1], k.shape[2]
+    pages = [(n + 127) // 128 for n in lens_k]
+    npg = sum(pages) + extra_pages
+    perm = torch.randperm(npg, generator=g)
+    kp = torch.randn(npg, hkv, 128, d, generator=g).to(k.dtype)
+    vp = torch.randn(npg, hkv, 128, d, generator=g).to(v.dtype)
+    pt = torch.zeros(len(lens_k), max(pages) + 1, dtype=torch.int32)
+    c = off = 0
+    for b, n in enumerate(lens_k):
+        for t in range(pages[b]):
+            p = int(perm[off])
+            off += 1
+            pt[b, t] = p
+            seg = slice(c + 128 * t, c + min(n, 128 * (t + 1)))
+            kp[p, :, :seg.stop - seg.start] = k[seg].permute(1, 0, 2)
+            vp[p, :, :seg.stop - seg.start] = v[seg].permute(1, 0, 2)
+        c += n
+    if bad_page:
+        pt[0, 1] = npg + 100  # unmapped page: contributes no keys
+    out = dict(inp_flat)
+    out.update(k=kp, v=vp, page_table=pt, seqused_k=torch.tensor(lens_k, dtype=torch.int32))
+    out.pop("cu_seqlens_k")
+    return out
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_prefill_paged(msa, kv):
+    lens_q, lens_k = [40, 300], [700, 300]
+    flat = _prefill_inputs(lens_q, lens_k, 8, 2, 5, seed=12, kv=kv)
+    inp = _paged(flat, lens_k, seed=3, bad_page=True)
+    out, lse = _run_prefill(msa, inp)
+    ref_out, ref_lse = _oracle(inp)
+    check_attention(out, lse, ref_out, ref_lse, label=f"paged_{kv}")
+
+
+def test_prefill_deterministic(msa):
+    inp = _prefill_inputs([700, 300], [700, 300], 8, 2, 6, seed=2)
+    o1, l1 = _run_prefill(msa, inp)
+    o2, l2 = _run_prefill(msa, inp)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ---------------------------------------------------------------- paged decode
+DECODE_CASES = [
+    # name, seqlen_q, seqused, hq, hkv, topk
+    ("sq1_g16", 1, [8192, 300, 129, 128, 1000], 32, 2, 16),
+    ("sq4_g16", 4, [5000, 300, 130, 4], 32, 2, 16),
+    ("sq2_g8", 2, [2000, 700], 16, 2, 8),
+    ("sq3_g4", 3, [1500, 257, 10], 8, 2, 5),
+    ("sq1_mha", 1, [600, 128], 4, 4, 3),
+    ("sq4_g16_topk64", 4, [20000], 16, 1, 64),
+]
+
+
+@pytest.mark.parametrize("case", DECODE_CASES, ids=[c[0] for c in DECODE_CASES])
+def test_decode_parity(msa, case):
+    name, sq, seqused, hq, hkv, topk = case
+    spec = workloads.DecodeSpec(name, len(seqused), (1, 1), hq, hkv, topk, seqlen_q=sq)
+    g = torch.Generator().manual_seed(len(name))
+    cu_q = torch.arange(0, len(seqused) * sq + 1, sq, dtype=torch.int32)
+    pages = [(n + 127) // 128 for n in seqused]
+    npg = sum(pages) + 3
+    perm = torch.randperm(npg, generator=g).to(torch.int32)
+    pt = torch.zeros(len(seqused), max(pages), dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(pages):
+        pt[b, :n] = perm[off:off + n]
+        off += n
+    k = torch.randn(npg, hkv, 128, 128, generator=g).to(torch.bfloat16)
+    v = torch.randn(npg, hkv, 128, 128, generator=g).to(torch.bfloat16)
+    q = torch.randn(len(seqused) * sq, hq, 128, generator=g).to(torch.bfloat16)
+    pos = workloads.query_positions(cu_q, seqused)
+    q2k = workloads.select_blocks(pos, hkv, topk, g)
+    q2k[0, 0, 0] = q2k[0, 0, 0]
+    if len(seqused) > 1:
+        pt[1, 0] = npg + 7  # an unmapped page
+    inp = dict(q=q, k=k, v=v, q2k_indices=q2k, cu_seqlens_q=cu_q, page_table=pt,
+               seqused_k=torch.tensor(seqused, dtype=torch.int32))
+    out, lse = _run_prefill(msa, inp, max_seqlen_q=sq)
+    ref_out, ref_lse = _oracle(inp)
+    check_attention(out, lse, ref_out, ref_lse, label=name)
+
+
+def test_decode_deterministic(msa):
+    g = torch.Generator().manual_seed(0)
+    seqused = [3000, 900]
+    cu_q = torch.arange(0, 2 * 4 + 1, 4, dtype=torch.int32)
+    pt = torch.arange(0, 48, dtype=torch.int32).view(2, 24)
+    k = torch.randn(48, 1, 128, 128, generator=g).to(torch.bfloat16)
+    v = torch.randn(48, 1, 128, 128, generator=g).to(torch.bfloat16)
+    q = torch.randn(8, 16, 128, generator=g).to(torch.bfloat16)
+    q2k = workloads.select_blocks(workloads.query_positions(cu_q, seqused), 1, 16, g)
+    inp = dict(q=q, k=k, v=v, q2k_indices=q2k, cu_seqlens_q=cu_q, page_table=pt,
+               seqused_k=torch.tensor(seqused, dtype=torch.int32))
+    o1, l1 = _run_prefill(msa, inp, max_seqlen_q=4)
+    o2, l2 = _run_prefill(msa, inp, max_seqlen_q=4)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ---------------------------------------------------------------- proxy score
+PROXY_CASES = [
+    # name, lens_q, lens_k, hq, hkv, reduce, causal, extra_tiles
+    ("reduce_g8", [300, 517], [300, 517], 16, 2, True, True, 0),
+    ("perhead_g8", [300], [300], 16, 2, False, True, 2),
+    ("reduce_g4_lq_lt_lk", [50, 129], [700, 129], 8, 2, True, True, 1),
+    ("reduce_mha", [400], [400], 2, 2, True, True, 0),
+    ("perhead_g3", [200], [260], 6, 2, False, True, 0),
+    ("reduce_g32", [300], [300], 32, 1, True, False, 0),
+]
+
+
+@pytest.mark.parametrize("case", PROXY_CASES, ids=[c[0] for c in PROXY_CASES])
+def test_proxy_parity(msa, case):
+    name, lq, lk, hq, hkv, red, causal, extra = case
+    g = torch.Generator().manual_seed(len(name) + 100)
+    q = torch.randn(sum(lq), hq, 128, generator=g).to(torch.bfloat16)
+    k = torch.randn(sum(lk), hkv, 128, generator=g).to(torch.bfloat16)
+    cu_q, cu_k = workloads.cu_from_lengths(lq), workloads.cu_from_lengths(lk)
+    T = max((n + 127) // 128 for n in lk) + extra
+    ref = oracle.proxy_score(q, k, cu_q, cu_k, causal=causal, max_k_tiles=T, reduce_heads=red)
+    got = msa.msa_proxy_score(q.to(DEV), k.to(DEV), cu_q.to(DEV), cu_k.to(DEV), causal=causal,
+                              max_k_tiles=T, reduce_heads=red)
+    torch.cuda.synchronize()
+    fault_clear(msa)
+    check_proxy(got, ref, label=name)
