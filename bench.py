@@ -188,8 +188,12 @@ def visible_counts(q2k, cu_q, k_lens, causal=True):
 
 
 # ---------------------------------------------------------------- headline: flat prefill
-def prefill_inputs(device, seed=0):
-    spec = workloads.FLAT_VARLEN
+PROFILE_SPEC = workloads.PrefillSpec("flat_prefill_1x8192_h64kv8_top16", [8192], 64, 8, 16,
+                                     first_prev=True)
+
+
+def prefill_inputs(device, seed=0, small=False):
+    spec = PROFILE_SPEC if small else workloads.FLAT_VARLEN
     inp = workloads.make_prefill(spec, seed, device=device)
     return spec, inp
 
@@ -226,7 +230,7 @@ def cpu_baseline_prefill(inp, rows_target=512, threads=None):
 
 
 def bench_prefill(msa, args, device, world, rank):
-    spec, inp = prefill_inputs(device)
+    spec, inp = prefill_inputs(device, small=args.profile_small)
     tq, hq, _ = inp["q"].shape
     hkv = inp["k"].shape[1]
     G = hq // hkv
@@ -286,6 +290,9 @@ def bench_prefill(msa, args, device, world, rank):
         work_efficiency=flops / flops_exec,
         union_blocks_per_tile=union_blocks / ulen.numel(),
     )
+    if args.profile_small:
+        res["e2e"] = None
+        return res
     # End-to-end through the public API with host buffers.
     host = {k: v.cpu().pin_memory() for k, v in inp.items()
             if torch.is_tensor(v) and k in ("q", "k", "v", "q2k_indices", "cu_seqlens_q",
@@ -492,6 +499,8 @@ def main():
     ap.add_argument("--impl", default="msa", choices=["msa", "reference"])
     ap.add_argument("--no-secondary", action="store_true", help="skip decode / two-stage")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-small", action="store_true",
+                    help="profiling case: prefill only, 1 x 8192 tokens, 64/8 heads, top-16")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -505,6 +514,8 @@ def main():
         dist.init_process_group("nccl", device_id=device)
     import block_sparse_top_msa_gb300 as msa
     msa.build()
+    if args.profile_small:
+        args.no_secondary = args.no_cpu_baseline = True
     res = bench_prefill(msa, args, device, world, rank)
     flush = l2_flush_buffer(device)
     secondary = {}
@@ -530,7 +541,8 @@ def main():
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(res["step_s"] * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": spec.name, "global_batch": 2 * world, "seq_len": 32768,
+            "config": {"workload": spec.name, "global_batch": len(spec.seqlens) * world,
+                       "seq_len": spec.seqlens[0],
                        "num_qo_heads": 64, "num_kv_heads": 8, "head_dim": 128, "topk": 16,
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (q 1.07 GB, k+v 268 MB, out 1.07 GB per step)"},

@@ -258,5 +258,8 @@ def msa_set_timing_events(events=None):
     if not events:
         _check("msa_set_timing_events", lib().msa_set_timing_events(None, 0))
         return
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event on first record
+            e.record()
     arr = (C.c_void_p * 3)(*[C.c_void_p(e.cuda_event) for e in events])
     _check("msa_set_timing_events", lib().msa_set_timing_events(arr, 3))
