@@ -69,6 +69,12 @@ def lib():
             vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
         L.msa_union_tile_tokens.restype = i32
         L.msa_union_tile_tokens.argtypes = [i32, i32]
+        L.msa_sparse_decode_noalloc.restype = i32
+        L.msa_sparse_decode_noalloc.argtypes = [
+            vp, vp, vp, vp, i32, vp, vp, i32, i32, vp, i32, i32, i32, i32, i32, i32, i32, f32,
+            vp, vp, vp]
+        L.msa_sparse_decode_noalloc_scratch_limit.restype = sz
+        L.msa_sparse_decode_noalloc_scratch_limit.argtypes = []
         L.msa_set_timing_events.restype = i32
         L.msa_set_timing_events.argtypes = [C.POINTER(C.c_void_p), i32]
         L.msa_read_device_fault.restype = i32
@@ -263,3 +269,28 @@ def msa_set_timing_events(events=None):
             e.record()
     arr = (C.c_void_p * 3)(*[C.c_void_p(e.cuda_event) for e in events])
     _check("msa_set_timing_events", lib().msa_set_timing_events(arr, 3))
+
+
+def msa_sparse_decode_noalloc(q, k, v, q2k_indices, cu_seqlens_q, page_table, seqused_k, *,
+                              max_seqlen_q, causal=True, softmax_scale=None, out=None, lse=None,
+                              stream=None):
+    """Paged decode that uses the library's fixed device scratch instead of a
+    workspace (for callers that cannot allocate); see include/msa.h."""
+    L = lib()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _cuda_contig(name, t, torch.bfloat16)
+    _cuda_contig("q2k_indices", q2k_indices, torch.int32)
+    _cuda_contig("cu_seqlens_q", cu_seqlens_q, torch.int32)
+    _cuda_contig("page_table", page_table, torch.int32)
+    _cuda_contig("seqused_k", seqused_k, torch.int32)
+    total_q, hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    st = L.msa_sparse_decode_noalloc(
+        _p(q), _p(k), _p(v), _p(q2k_indices), q2k_indices.shape[2], _p(cu_seqlens_q),
+        _p(page_table), page_table.shape[1], k.shape[0], _p(seqused_k),
+        cu_seqlens_q.shape[0] - 1, total_q, hq, k.shape[1], d, int(max_seqlen_q),
+        int(bool(causal)), float(softmax_scale) if softmax_scale is not None else 0.0, _p(out),
+        _p(lse), _stream(stream))
+    _check("msa_sparse_decode_noalloc", st)
+    return (out, lse) if lse is not None else out

@@ -183,6 +183,40 @@ int msa_union_tile_tokens(int num_qo_heads, int num_kv_heads);
 msa_status_t msa_read_device_fault(unsigned int* fault, cudaStream_t stream);
 
 /*
+ * Paged decode for callers that cannot allocate device memory (no counterpart
+ * on the documentation pages; it is an addition of this library).
+ *
+ * Engines that plan all device memory ahead of time, plugin interfaces that
+ * give a kernel no workspace, and code running where cudaMalloc may not be
+ * called cannot provide the workspace msa_sparse_attention_fwd needs. This
+ * entry point computes the same result as msa_sparse_attention_fwd on its
+ * split-KV decode route (paged bf16 K/V, max_seqlen_q <= 4, G <= 16,
+ * head_dim 128, topk <= 64; arguments as there, q and K/V bf16) but keeps its
+ * scratch in a fixed 16 MiB array inside the library's device image, which
+ * every GPU that loads the library holds until the process exits. It
+ * allocates nothing. The scratch it needs is
+ *   align256(P * R * 512) + align256(P * R * 8) + align256(batch * Hkv * 4) bytes,
+ * R = 16, 32 or 64 (s_q * G rounded up), P = batch * Hkv * ceil(s_q * topk / S),
+ * S = 4 pages per split when s_q * G <= 16 and 8 otherwise; larger problems
+ * are rejected with MSA_WORKSPACE_TOO_SMALL before anything is launched.
+ * msa_sparse_decode_noalloc_scratch_limit() returns the array size.
+ *
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture. All calls share the one array and it keeps the previous call's
+ * contents: the completion tickets are cleared on `stream` before every
+ * launch, and calls whose work overlaps on the GPU race on the array, so
+ * callers must order them.
+ */
+msa_status_t msa_sparse_decode_noalloc(
+    const void* q, const void* k, const void* v, const int32_t* q2k_indices, int topk,
+    const int32_t* cu_seqlens_q, const int32_t* page_table, int max_pages, int num_pages,
+    const int32_t* seqused_k, int batch, int total_q, int num_qo_heads, int num_kv_heads,
+    int head_dim, int max_seqlen_q, int causal, float softmax_scale, void* out, float* lse,
+    cudaStream_t stream);
+size_t msa_sparse_decode_noalloc_scratch_limit(void);
+
+/*
  * Diagnostics: timing events for msa_sparse_attention_fwd. When `events`
  * points to three cudaEvent_t handles (count == 3), every later forward call
  * records events[0] before its first launch, events[1] after the metadata
