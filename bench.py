@@ -330,11 +330,15 @@ def bench_prefill(msa, args, device, world, rank):
 
 
 # ---------------------------------------------------------------- secondary: paged decode
-def bench_decode(msa, device, flush, seed=0):
-    spec = workloads.PAGED_DECODE
+DECODE_PROFILE_SPEC = workloads.DecodeSpec("paged_decode_b32_U[8192,32768]_h64kv4_top16", 32,
+                                           (8192, 32768), 64, 4, 16)
+
+
+def bench_decode(msa, device, flush, seed=0, small=False, sqs=(1, 4), reps=7):
+    spec = DECODE_PROFILE_SPEC if small else workloads.PAGED_DECODE
     out = {}
     pk = peaks()
-    for sq in (1, 4):
+    for sq in sqs:
         inp = workloads.make_decode(spec, seed, device=device, seqlen_q=sq)
         q2k, pt, su = inp["q2k_indices"], inp["page_table"], inp["seqused_k"]
         hkv = inp["k"].shape[1]
@@ -366,22 +370,25 @@ def bench_decode(msa, device, flush, seed=0):
         for _ in range(3):
             call()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-        ts = []
-        for _ in range(7):
+        ts, ta = [], []
+        for _ in range(reps):
             flush.fill_(1)
             msa.msa_set_timing_events(ev)
             call()
             ev[2].synchronize()
-            ts.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+            ts.append(ev[0].elapsed_time(ev[2]) * 1e-3)
+            ta.append(ev[1].elapsed_time(ev[2]) * 1e-3)
         msa.msa_set_timing_events(None)
-        t = statistics.median(ts)
+        t, t_attn = statistics.median(ts), statistics.median(ta)
         gbs = (kv_bytes + meta) / t / 1e9
+        gbs_attn = (kv_bytes + meta) / t_attn / 1e9
         out[f"seqlen_q_{sq}"] = {
             "value": round(gbs, 1), "unit": "GB/s", "us": round(t * 1e6, 2),
+            "attention_us": round(t_attn * 1e6, 2),
             "kv_bytes": int(kv_bytes), "meta_bytes": int(meta),
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"],
-                         "unit": "GB/s", "frac": round(gbs / pk["hbm"], 4), "traffic": None,
-                         "kernel": "decode_kernel"}}
+            "roofline": {"bound": "hbm", "achieved": round(gbs_attn, 1), "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": round(gbs_attn / pk["hbm"], 4), "traffic": None,
+                         "kernel": "prefill_kernel<bf16> (paged, split items)"}}
         del inp
         torch.cuda.empty_cache()
     out["workload"] = spec.name
@@ -501,6 +508,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-small", action="store_true",
                     help="profiling case: prefill only, 1 x 8192 tokens, 64/8 heads, top-16")
+    ap.add_argument("--profile-decode", type=int, default=0, metavar="SQ",
+                    help="profiling case: paged decode only, 32 requests, seqlen_q SQ")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -514,6 +523,12 @@ def main():
         dist.init_process_group("nccl", device_id=device)
     import block_sparse_top_msa_gb300 as msa
     msa.build()
+    if args.profile_decode:
+        flush = l2_flush_buffer(device)
+        r = bench_decode(msa, device, flush, small=True, sqs=(args.profile_decode,),
+                         reps=args.steps)
+        print(json.dumps({"profile_decode": r}))
+        return 0
     if args.profile_small:
         args.no_secondary = args.no_cpu_baseline = True
     res = bench_prefill(msa, args, device, world, rank)

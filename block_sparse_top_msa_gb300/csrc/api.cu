@@ -31,8 +31,6 @@ unsigned* fault_word() {
 namespace {
 
 constexpr int kMaxTopk = 64;
-constexpr int kDecodeMaxSq = 4;
-constexpr int kDecodeMaxGroup = 16;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -43,56 +41,67 @@ int tile_tokens_for(int hq, int hkv) {
   return G >= 128 ? 1 : 128 / G;
 }
 
+// Work items the persistent attention kernel aims for (about 8 per SM of a
+// 152-SM GB300); fewer (tile, KV head) units than this split their union lists.
+constexpr int kTargetItems = 8 * 152;
+constexpr int kMinSplitBlocks = 8;
+
 struct PrefillLayout {
   int W, max_tiles, cap, words;
-  size_t off_info, off_len, off_blocks, off_member, total;
+  int splits, pps, rows_part, num_items;
+  size_t off_info, off_len, off_blocks, off_member, off_part_o, off_part_ml, off_tickets, total;
 };
 
-PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk) {
+PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk, int max_seqlen_q) {
   PrefillLayout L{};
   L.W = tile_tokens_for(hq, hkv);
   L.max_tiles = (total_q + L.W - 1) / L.W + batch;
   L.cap = L.W * topk;
   L.words = (L.cap + 31) / 32;
+  const int G = hq / hkv;
+  const long long units = (long long)hkv * L.max_tiles;
+  const int sq = max_seqlen_q < 1 ? 1 : max_seqlen_q;
+  // Longest union a tile can have: its tokens' selections, at most cap.
+  const int bound = (int)((long long)(sq < L.W ? sq : L.W) * topk < L.cap
+                              ? (long long)(sq < L.W ? sq : L.W) * topk
+                              : L.cap);
+  L.splits = 1;
+  L.pps = L.cap;
+  if (units < kTargetItems) {
+    int S = (int)((kTargetItems + units - 1) / units);
+    if (S > bound) S = bound;
+    if (S > 1) {
+      // At least kMinSplitBlocks blocks per item, so per-item work (Q load,
+      // partial write, merge) stays small next to the K/V stream.
+      L.pps = (bound + S - 1) / S;
+      if (L.pps < kMinSplitBlocks) L.pps = kMinSplitBlocks;
+      L.splits = (bound + L.pps - 1) / L.pps;
+      if (L.splits == 1) L.pps = L.cap;
+    }
+  }
+  L.rows_part = 0;
+  if (L.splits > 1) {
+    const int rows = (sq < L.W ? sq : L.W) * G;
+    L.rows_part = rows >= 128 ? 128 : ((rows + 15) / 16) * 16;
+  }
+  L.num_items = (int)(units * L.splits);
   size_t off = 0;
   L.off_info = off;
   off += up256((size_t)L.max_tiles * 2 * sizeof(int32_t));
   L.off_len = off;
-  off += up256((size_t)hkv * L.max_tiles * sizeof(int32_t));
+  off += up256((size_t)units * sizeof(int32_t));
   L.off_blocks = off;
-  off += up256((size_t)hkv * L.max_tiles * L.cap * sizeof(int32_t));
+  off += up256((size_t)units * L.cap * sizeof(int32_t));
   L.off_member = off;
-  off += up256((size_t)hkv * L.max_tiles * L.W * L.words * sizeof(uint32_t));
-  L.total = off;
-  return L;
-}
-
-struct DecodeLayout {
-  int rows, pps, splits;
-  size_t off_o, off_ml, off_tickets, total;
-};
-
-DecodeLayout decode_layout(int batch, int hq, int hkv, int topk, int sq_max) {
-  DecodeLayout L{};
-  const int G = hq / hkv;
-  L.rows = G * sq_max;
-  const int R = L.rows <= 16 ? 16 : (L.rows <= 32 ? 32 : 64);
-  L.pps = decode_pages_per_split(L.rows);
-  L.splits = (sq_max * topk + L.pps - 1) / L.pps;
-  const size_t parts = (size_t)batch * hkv * L.splits;
-  size_t off = 0;
-  L.off_o = off;
-  off += up256(parts * R * 128 * sizeof(float));
-  L.off_ml = off;
-  off += up256(parts * R * 2 * sizeof(float));
+  off += up256((size_t)units * L.W * L.words * sizeof(uint32_t));
+  L.off_part_o = off;
+  off += up256((size_t)units * L.splits * L.rows_part * 128 * sizeof(float));
+  L.off_part_ml = off;
+  off += up256((size_t)units * L.splits * L.rows_part * 2 * sizeof(float));
   L.off_tickets = off;
-  off += up256((size_t)batch * hkv * sizeof(int));
+  off += up256((size_t)units * sizeof(int));
   L.total = off;
   return L;
-}
-
-bool use_decode(bool paged, int max_seqlen_q, int G, msa_dtype_t kv_dtype) {
-  return paged && max_seqlen_q <= kDecodeMaxSq && G <= kDecodeMaxGroup && kv_dtype == MSA_BF16;
 }
 
 // (d, H, T) map over a (T, H, d) tensor; element size 2 (bf16) or 1 (e4m3).
@@ -152,13 +161,8 @@ size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_he
       num_qo_heads % num_kv_heads != 0 || head_dim != 128 || topk < 1 || topk > kMaxTopk ||
       num_qo_heads / num_kv_heads > 128)
     return 0;
-  size_t bytes = prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk).total;
-  const int G = num_qo_heads / num_kv_heads;
-  if (paged && max_seqlen_q >= 1 && max_seqlen_q <= kDecodeMaxSq && G <= kDecodeMaxGroup) {
-    const size_t d = decode_layout(batch, num_qo_heads, num_kv_heads, topk, max_seqlen_q).total;
-    if (d > bytes) bytes = d;
-  }
-  return bytes;
+  (void)paged;
+  return prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q).total;
 }
 
 msa_status_t msa_sparse_attention_fwd(
@@ -204,45 +208,8 @@ msa_status_t msa_sparse_attention_fwd(
   const int esize = kv_dtype == MSA_FP8_E4M3 ? 1 : 2;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
 
-  if (use_decode(paged, max_seqlen_q, G, kv_dtype)) {
-    const DecodeLayout L = decode_layout(batch, num_qo_heads, num_kv_heads, topk, max_seqlen_q);
-    DecodeArgs a{};
-    a.fault = fault;
-    if (!map_rows(&a.tmap_q, q, 2, num_qo_heads, total_q, (uint32_t)G, (uint32_t)max_seqlen_q) ||
-        !map_pages(&a.tmap_k, k, 2, num_kv_heads, num_pages) ||
-        !map_pages(&a.tmap_v, v, 2, num_kv_heads, num_pages))
-      return MSA_CUDA_ERROR;
-    a.q2k = q2k_indices;
-    a.topk = topk;
-    a.cu_q = cu_seqlens_q;
-    a.page_table = page_table;
-    a.max_pages = max_pages;
-    a.num_pages = num_pages;
-    a.seqused_k = seqused_k;
-    a.batch = batch;
-    a.total_q = total_q;
-    a.num_qo_heads = num_qo_heads;
-    a.num_kv_heads = num_kv_heads;
-    a.sq_max = max_seqlen_q;
-    a.causal = causal ? 1 : 0;
-    a.scale_log2 = scale_log2;
-    a.out = out;
-    a.lse = lse;
-    a.pages_per_split = L.pps;
-    a.splits = L.splits;
-    a.part_o = reinterpret_cast<float*>(ws + L.off_o);
-    a.part_ml = reinterpret_cast<float*>(ws + L.off_ml);
-    a.tickets = reinterpret_cast<int*>(ws + L.off_tickets);
-    mark(0, stream);
-    cudaError_t e = cudaMemsetAsync(a.tickets, 0, (size_t)batch * num_kv_heads * sizeof(int), stream);
-    if (e != cudaSuccess) return MSA_CUDA_ERROR;
-    mark(1, stream);
-    e = launch_decode(a, stream);
-    mark(2, stream);
-    return from_cuda(e);
-  }
-
-  const PrefillLayout L = prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk);
+  const PrefillLayout L =
+      prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q);
   UnionArgs u{};
   u.q2k = q2k_indices;
   u.topk = topk;
@@ -265,6 +232,11 @@ msa_status_t msa_sparse_attention_fwd(
   mark(0, stream);
   cudaError_t e = launch_build_union(u, stream);
   if (e != cudaSuccess) return MSA_CUDA_ERROR;
+  if (L.splits > 1) {
+    e = cudaMemsetAsync(ws + L.off_tickets, 0,
+                        (size_t)num_kv_heads * L.max_tiles * sizeof(int), stream);
+    if (e != cudaSuccess) return MSA_CUDA_ERROR;
+  }
   mark(1, stream);
 
   PrefillArgs a{};
@@ -302,6 +274,13 @@ msa_status_t msa_sparse_attention_fwd(
   a.tile_info = u.tile_info;
   a.out = out;
   a.lse = lse;
+  a.splits = L.splits;
+  a.pps = L.pps;
+  a.rows_part = L.rows_part;
+  a.num_items = L.num_items;
+  a.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
+  a.part_ml = reinterpret_cast<float*>(ws + L.off_part_ml);
+  a.tickets = reinterpret_cast<int*>(ws + L.off_tickets);
   e = launch_prefill(a, stream);
   mark(2, stream);
   return from_cuda(e);

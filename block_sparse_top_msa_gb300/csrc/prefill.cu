@@ -32,32 +32,42 @@
 namespace msa {
 namespace {
 
-constexpr int kStages = 2;      // bf16 K/V ring
-constexpr int kF8Stages = 2;    // E4M3 staging ring
+constexpr int kKStages = 2;     // K ring (a slot frees when its QK completes)
+constexpr int kF8Stages = 2;    // E4M3 staging ring (K and V bytes of one block)
+constexpr int kSBuf = 3;        // S/P buffers in TMEM: QK runs two blocks ahead of PV
 constexpr int kTile = 16384;    // bytes of one 128-row x 128-byte swizzled tile
 constexpr float kRescaleLog2 = 8.0f;
 
-// TMEM column map (512 columns allocated).
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP0 = 384, kColP1 = 448;
+// TMEM column map (512 columns allocated): S_b at 128*b for b = 0..2 (its P,
+// packed bf16 pairs, overwrites the first 64 columns of S_b once the softmax
+// has read S_b), O at 384.
+constexpr uint32_t kColO = 384;
 
 template <bool FP8>
 struct __align__(1024) PrefillSmem {
-  uint8_t q[2][kTile];
-  uint8_t k[kStages][2][kTile];
-  uint8_t v[kStages][2][kTile];
+  static constexpr int kQBuf = FP8 ? 1 : 2;     // Q tiles of consecutive work items
+  static constexpr int kVStages = FP8 ? 2 : 3;  // V ring (a slot frees when its PV completes)
+  uint8_t q[kQBuf][2][kTile];
+  uint8_t k[kKStages][2][kTile];
+  uint8_t v[kVStages][2][kTile];
   uint8_t k8[FP8 ? kF8Stages : 1][FP8 ? kTile : 16];
   uint8_t v8[FP8 ? kF8Stages : 1][FP8 ? kTile : 16];
-  uint64_t q_full;
-  uint64_t k_full[kStages];
-  uint64_t v_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t q_full[kQBuf];
+  uint64_t q_empty[kQBuf];
+  uint64_t k_full[kKStages];
+  uint64_t k_empty[kKStages];
+  uint64_t v_full[kVStages];
+  uint64_t v_empty[kVStages];
   uint64_t f8_full[kF8Stages];
   uint64_t f8_empty[kF8Stages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t s_full[kSBuf];
+  uint64_t p_full[kSBuf];
   uint64_t o_done[2];
+  uint64_t o_free;
+  uint64_t ep_bar;
   uint64_t drain;
   uint32_t tmem_base;
+  int ticket_last;
   int abort;
 };
 
@@ -75,6 +85,61 @@ MSA_DEV float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+MSA_DEV float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Max of 64 values with four independent three-input chains.
+MSA_DEV float row_max64(const float* v) {
+  float m0 = v[0], m1 = v[1], m2 = v[2], m3 = v[3];
+#pragma unroll
+  for (int c = 4; c + 8 <= 64; c += 8) {
+    m0 = fmax3(m0, v[c], v[c + 1]);
+    m1 = fmax3(m1, v[c + 2], v[c + 3]);
+    m2 = fmax3(m2, v[c + 4], v[c + 5]);
+    m3 = fmax3(m3, v[c + 6], v[c + 7]);
+  }
+  m0 = fmax3(m0, v[60], v[61]);
+  m1 = fmax3(m1, v[62], v[63]);
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+MSA_DEV float row_max128(const float* v) { return fmaxf(row_max64(v), row_max64(v + 64)); }
+
+// Running-max update of one row for a block whose raw max logit is mx. The
+// reference max only moves when the new max exceeds it by more than 2^8, so
+// O is rescaled rarely; P stays <= 2^8, exact enough for bf16 and fp32 sums.
+MSA_DEV void update_max(bool mem, float mx, float scale_log2, float& m_ref, float& l,
+                        float& alpha, bool& rescale) {
+  if (!mem) return;
+  const float m_new = mx * scale_log2;
+  if (m_ref == -INFINITY || m_new > m_ref + kRescaleLog2) {
+    if (m_ref != -INFINITY) {
+      alpha = ex2(m_ref - m_new);
+      rescale = true;
+      l *= alpha;
+    }
+    m_ref = m_new;
+  }
+}
+
+// P = 2^(s * scale_log2 + neg_m) for N columns, packed to bf16 pairs and
+// stored to TMEM at pcol (N/2 columns); the fp32 values are summed into acc.
+template <int N>
+MSA_DEV void exp_pack_store(const float* sv, float2 sc2, float neg_m, float2& acc, uint32_t pcol) {
+  uint32_t pk[N / 2];
+  const float2 nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+  for (int c = 0; c < N; c += 2) {
+    const float2 x = __ffma2_rn(make_float2(sv[c], sv[c + 1]), sc2, nm2);
+    const float p0 = ex2(x.x), p1 = ex2(x.y);
+    acc = __fadd2_rn(acc, make_float2(p0, p1));
+    pk[c >> 1] = pack_bf16x2(p0, p1);
+  }
+  if (N == 64) tmem_st32(pcol, pk);
 }
 
 // Upconverts one 128x128 E4M3 tile (TMA SWIZZLE_128B image, 128-byte rows)
@@ -108,49 +173,116 @@ MSA_DEV void convert_tile(const uint8_t* src, uint8_t* dst_half0, int t) {
   }
 }
 
+// One work item: a (query tile, KV head, split) triple and its slice of the
+// tile's union list. Every role derives the same items in the same order.
+struct Item {
+  int tile, h, split, t0, b, n_union, p_begin, n;
+  int seq_q0, lq, lk, kv0;  // the tile's sequence (valid when t0 >= 0)
+};
+
+MSA_DEV Item item_at(const PrefillArgs& a, int i) {
+  const int per_tile = a.num_kv_heads * a.splits;
+  const int tile_idx = i / per_tile;
+  const int rem = i - tile_idx * per_tile;
+  Item it;
+  it.tile = a.max_tiles - 1 - tile_idx;  // later (heavier) tiles first
+  it.h = rem / a.splits;
+  it.split = rem - it.h * a.splits;
+  it.t0 = __ldg(a.tile_info + 2 * it.tile);
+  it.b = __ldg(a.tile_info + 2 * it.tile + 1);
+  it.p_begin = it.split * a.pps;
+  it.n_union = 0;
+  it.n = 0;
+  it.seq_q0 = it.lq = it.lk = it.kv0 = 0;
+  if (it.t0 >= 0) {
+    it.n_union = __ldg(a.union_len + (size_t)it.h * a.max_tiles + it.tile);
+    it.n = max(0, min(it.n_union, it.p_begin + a.pps) - it.p_begin);
+    it.seq_q0 = __ldg(a.cu_q + it.b);
+    it.lq = __ldg(a.cu_q + it.b + 1) - it.seq_q0;
+    if (a.paged) {
+      it.lk = __ldg(a.seqused_k + it.b);
+    } else {
+      it.kv0 = __ldg(a.cu_k + it.b);
+      it.lk = __ldg(a.cu_k + it.b + 1) - it.kv0;
+    }
+  }
+  return it;
+}
+
+// Position in the CTA's stream of blocks: item index i (stride gridDim.x),
+// block u inside the item, ordinal k of the item among non-empty items, and
+// global block ordinal g.
+struct Cursor {
+  int i, u, k, g;
+  bool valid;
+  Item it;
+};
+
+MSA_DEV void cursor_next(const PrefillArgs& a, Cursor& c) {
+  ++c.g;
+  ++c.u;
+  while (c.u >= c.it.n) {
+    c.i += gridDim.x;
+    if (c.i >= a.num_items) {
+      c.valid = false;
+      return;
+    }
+    c.it = item_at(a, c.i);
+    c.u = 0;
+    if (c.it.n > 0) ++c.k;
+  }
+  c.valid = true;
+}
+
+MSA_DEV void cursor_begin(const PrefillArgs& a, Cursor& c) {
+  c.i = (int)blockIdx.x - (int)gridDim.x;
+  c.u = 0;
+  c.k = -1;
+  c.g = -1;
+  c.it.n = 0;
+  cursor_next(a, c);
+}
+
 template <bool FP8>
 __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a) {
   using R = Roles<FP8>;
   using Smem = PrefillSmem<FP8>;
+  constexpr int kQBuf = Smem::kQBuf;
+  constexpr int kVStages = Smem::kVStages;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                       ~uintptr_t(1023));
   unsigned* fault = a.fault;
   volatile int* abort = &sm.abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = a.max_tiles - 1 - (int)blockIdx.x;  // heavier (later) tiles first
-  const int h = blockIdx.y;
   const int G = a.num_qo_heads / a.num_kv_heads;
   const int W = a.tile_tokens;
 
-  const int t0 = a.tile_info[2 * tile];
-  if (t0 < 0) return;  // past the last tile (uniform over the CTA)
-  const int b = a.tile_info[2 * tile + 1];
-  const size_t ubase = (size_t)h * a.max_tiles + tile;
-  const int n = a.union_len[ubase];
-  const int32_t* ulist = a.union_blocks + ubase * a.cap;
-  const int seq_q0 = a.cu_q[b];
-  const int lq = a.cu_q[b + 1] - seq_q0;
-  const int lk = a.paged ? a.seqused_k[b] : a.cu_k[b + 1] - a.cu_k[b];
-  const int nw = min(W, seq_q0 + lq - t0);
-
   if (tid == 0) {
-    mbar_init(&sm.q_full, 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kQBuf; ++s) {
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);
+    }
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&sm.k_full[s], FP8 ? 4 : 1);
+      mbar_init(&sm.k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&sm.v_full[s], FP8 ? 4 : 1);
-      mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
     }
     for (int s = 0; s < kF8Stages; ++s) {
       mbar_init(&sm.f8_full[s], 1);
       mbar_init(&sm.f8_empty[s], 4);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kSBuf; ++s) {
       mbar_init(&sm.s_full[s], 1);
       mbar_init(&sm.p_full[s], 4);
-      mbar_init(&sm.o_done[s], 1);
     }
+    for (int s = 0; s < 2; ++s) mbar_init(&sm.o_done[s], 1);
+    mbar_init(&sm.o_free, 4);
+    mbar_init(&sm.ep_bar, 4);
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
     fence_mbar_init();
@@ -166,112 +298,156 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
 
   if (warp == R::kProducerWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       tma_prefetch_desc(&a.tmap_q);
       tma_prefetch_desc(&a.tmap_k);
       tma_prefetch_desc(&a.tmap_v);
-      mbar_expect_tx(&sm.q_full, 2u * 128u * (uint32_t)(G * W));
-      for (int c = 0; c < 2; ++c) tma_load_3d(sm.q[c], &a.tmap_q, &sm.q_full, c * 64, h * G, t0);
-      const int kv0 = a.paged ? 0 : a.cu_k[b];
-      int last_issue[kStages > kF8Stages ? kStages : kF8Stages];
-      for (int s = 0; s < (kStages > kF8Stages ? kStages : kF8Stages); ++s) last_issue[s] = -1;
+      // Last block issued into each slot, to drain copies in flight on abort.
+      int last_k[kKStages], last_v[kVStages], last_8[kF8Stages];
+      for (int s = 0; s < kKStages; ++s) last_k[s] = -1;
+      for (int s = 0; s < kVStages; ++s) last_v[s] = -1;
+      for (int s = 0; s < kF8Stages; ++s) last_8[s] = -1;
       bool ok = true;
-      for (int u = 0; u < n; ++u) {
-        const int blk = ulist[u];
-        int page = 0;
-        if (a.paged) {
-          page = a.page_table[(size_t)b * a.max_pages + blk];
-          // An unmapped page reads as zeros (out-of-range TMA box) and is masked.
-          if (page < 0 || page >= a.num_pages) page = a.num_pages;
+      int g = 0, k = 0;  // blocks issued, non-empty items seen
+      for (int i = blockIdx.x; ok && i < a.num_items; i += gridDim.x) {
+        const Item it = item_at(a, i);
+        if (it.n == 0) continue;
+        const int qb = k % kQBuf;
+        if (k >= kQBuf &&
+            !mbar_wait(&sm.q_empty[qb], ((k / kQBuf) - 1) & 1, fault, kFaultWaitMma, abort)) {
+          ok = false;
+          break;
         }
-        if (!FP8) {
-          const int st = u % kStages;
-          if (u >= kStages &&
-              !mbar_wait(&sm.kv_empty[st], ((u / kStages) - 1) & 1, fault, kFaultWaitMma, abort)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(&sm.k_full[st], 2 * kTile);
-          for (int c = 0; c < 2; ++c) {
-            if (a.paged) tma_load_4d(sm.k[st][c], &a.tmap_k, &sm.k_full[st], c * 64, 0, h, page);
-            else tma_load_3d(sm.k[st][c], &a.tmap_k, &sm.k_full[st], c * 64, h, kv0 + blk * kBlk);
-          }
-          mbar_expect_tx(&sm.v_full[st], 2 * kTile);
-          for (int c = 0; c < 2; ++c) {
-            if (a.paged) tma_load_4d(sm.v[st][c], &a.tmap_v, &sm.v_full[st], c * 64, 0, h, page);
-            else tma_load_3d(sm.v[st][c], &a.tmap_v, &sm.v_full[st], c * 64, h, kv0 + blk * kBlk);
-          }
-          last_issue[st] = u;
-        } else {
-          const int s8 = u % kF8Stages;
-          if (u >= kF8Stages &&
-              !mbar_wait(&sm.f8_empty[s8], ((u / kF8Stages) - 1) & 1, fault, kFaultWaitOther,
-                         abort)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(&sm.f8_full[s8], 2 * kTile);
+        mbar_expect_tx(&sm.q_full[qb], 2u * 128u * (uint32_t)(G * W));
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(sm.q[qb][c], &a.tmap_q, &sm.q_full[qb], c * 64, it.h * G, it.t0);
+        const int32_t* ulist =
+            a.union_blocks + ((size_t)it.h * a.max_tiles + it.tile) * a.cap + it.p_begin;
+        for (int u = 0; u < it.n; ++u, ++g) {
+          const int blk = ulist[u];
+          int page = 0;
           if (a.paged) {
-            tma_load_4d(sm.k8[s8], &a.tmap_k, &sm.f8_full[s8], 0, 0, h, page);
-            tma_load_4d(sm.v8[s8], &a.tmap_v, &sm.f8_full[s8], 0, 0, h, page);
-          } else {
-            tma_load_3d(sm.k8[s8], &a.tmap_k, &sm.f8_full[s8], 0, h, kv0 + blk * kBlk);
-            tma_load_3d(sm.v8[s8], &a.tmap_v, &sm.f8_full[s8], 0, h, kv0 + blk * kBlk);
+            page = a.page_table[(size_t)it.b * a.max_pages + blk];
+            // An unmapped page reads as zeros (out-of-range TMA box) and is masked.
+            if (page < 0 || page >= a.num_pages) page = a.num_pages;
           }
-          last_issue[s8] = u;
+          const int row = it.kv0 + blk * kBlk;
+          if (!FP8) {
+            const int ks = g % kKStages, vs = g % kVStages;
+            if (g >= kKStages && !mbar_wait(&sm.k_empty[ks], ((g / kKStages) - 1) & 1, fault,
+                                            kFaultWaitMma, abort)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&sm.k_full[ks], 2 * kTile);
+            for (int c = 0; c < 2; ++c) {
+              if (a.paged) tma_load_4d(sm.k[ks][c], &a.tmap_k, &sm.k_full[ks], c * 64, 0, it.h, page);
+              else tma_load_3d(sm.k[ks][c], &a.tmap_k, &sm.k_full[ks], c * 64, it.h, row);
+            }
+            last_k[ks] = g;
+            if (g >= kVStages && !mbar_wait(&sm.v_empty[vs], ((g / kVStages) - 1) & 1, fault,
+                                            kFaultWaitMma, abort)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&sm.v_full[vs], 2 * kTile);
+            for (int c = 0; c < 2; ++c) {
+              if (a.paged) tma_load_4d(sm.v[vs][c], &a.tmap_v, &sm.v_full[vs], c * 64, 0, it.h, page);
+              else tma_load_3d(sm.v[vs][c], &a.tmap_v, &sm.v_full[vs], c * 64, it.h, row);
+            }
+            last_v[vs] = g;
+          } else {
+            const int s8 = g % kF8Stages;
+            if (g >= kF8Stages && !mbar_wait(&sm.f8_empty[s8], ((g / kF8Stages) - 1) & 1, fault,
+                                             kFaultWaitOther, abort)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&sm.f8_full[s8], 2 * kTile);
+            if (a.paged) {
+              tma_load_4d(sm.k8[s8], &a.tmap_k, &sm.f8_full[s8], 0, 0, it.h, page);
+              tma_load_4d(sm.v8[s8], &a.tmap_v, &sm.f8_full[s8], 0, 0, it.h, page);
+            } else {
+              tma_load_3d(sm.k8[s8], &a.tmap_k, &sm.f8_full[s8], 0, it.h, row);
+              tma_load_3d(sm.v8[s8], &a.tmap_v, &sm.f8_full[s8], 0, it.h, row);
+            }
+            last_8[s8] = g;
+          }
         }
+        ++k;
       }
       if (!ok) {
         // Let copies already in flight land before the CTA's shared memory is released.
-        for (int s = 0; s < (FP8 ? kF8Stages : kStages); ++s) {
-          const int u = last_issue[s];
-          if (u < 0) continue;
-          if (FP8) {
-            mbar_wait(&sm.f8_full[s], (u / kF8Stages) & 1, fault, kFaultWaitTma);
-          } else {
-            mbar_wait(&sm.k_full[s], (u / kStages) & 1, fault, kFaultWaitTma);
-            mbar_wait(&sm.v_full[s], (u / kStages) & 1, fault, kFaultWaitTma);
-          }
-        }
+        for (int s = 0; s < kKStages; ++s)
+          if (last_k[s] >= 0) mbar_wait(&sm.k_full[s], (last_k[s] / kKStages) & 1, fault, kFaultWaitTma);
+        for (int s = 0; s < kVStages; ++s)
+          if (last_v[s] >= 0) mbar_wait(&sm.v_full[s], (last_v[s] / kVStages) & 1, fault, kFaultWaitTma);
+        for (int s = 0; s < kF8Stages; ++s)
+          if (last_8[s] >= 0) mbar_wait(&sm.f8_full[s], (last_8[s] / kF8Stages) & 1, fault, kFaultWaitTma);
       }
     }
   } else if (warp == R::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
+    // Walks the block stream twice: QK runs two blocks ahead of PV, across
+    // item boundaries, so the softmax of block g overlaps PV(g-1) and QK(g+1).
+    if (lane == 0) {
       const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       const uint32_t idO = idesc_bf16_f32(128, 128, false, true);
-      bool ok = mbar_wait(&sm.q_full, 0, fault, kFaultWaitTma, abort);
-      auto pv = [&](int u) -> bool {
-        const int bb = u & 1, st = u % kStages;
-        if (!mbar_wait(&sm.p_full[bb], (u >> 1) & 1, fault, kFaultWaitSoftmax, abort)) return false;
-        if (!mbar_wait(&sm.v_full[st], (u / kStages) & 1, fault, kFaultWaitTma, abort)) return false;
+      bool ok = true;
+      auto issue_qk = [&](const Cursor& c) -> bool {
+        const int qb = c.k % kQBuf, ks = c.g % kKStages, b = c.g % kSBuf;
+        if (c.u == 0 && !mbar_wait(&sm.q_full[qb], (c.k / kQBuf) & 1, fault, kFaultWaitTma, abort))
+          return false;
+        if (!mbar_wait(&sm.k_full[ks], (c.g / kKStages) & 1, fault, kFaultWaitTma, abort))
+          return false;
         tc_fence_after();
-        const uint32_t pcol = bb ? kColP1 : kColP0;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t bd = sdesc_sw128(smem_u32(sm.v[st][0]) + k * 2048, kTile, 1024);
-          mma_ts(tbase + kColO, tbase + pcol + k * 8, bd, idO, (u > 0 || k > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t ad = sdesc_sw128(smem_u32(sm.q[qb][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(smem_u32(sm.k[ks][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          mma_ss(tbase + b * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&sm.o_done[bb]);
-        mma_commit(&sm.kv_empty[st]);
+        mma_commit(&sm.s_full[b]);
+        mma_commit(&sm.k_empty[ks]);
+        if (c.u == c.it.n - 1) mma_commit(&sm.q_empty[qb]);
         return true;
       };
-      for (int u = 0; ok && u < n; ++u) {
-        const int bb = u & 1, st = u % kStages;
-        ok = mbar_wait(&sm.k_full[st], (u / kStages) & 1, fault, kFaultWaitTma, abort);
-        if (!ok) break;
+      auto issue_pv = [&](const Cursor& c) -> bool {
+        const int b = c.g % kSBuf, vs = c.g % kVStages;
+        // A new item's first PV overwrites O: its previous epilogue must have read it.
+        if (c.u == 0 && c.k > 0 &&
+            !mbar_wait(&sm.o_free, (c.k - 1) & 1, fault, kFaultWaitSoftmax, abort))
+          return false;
+        if (!mbar_wait(&sm.p_full[b], (c.g / kSBuf) & 1, fault, kFaultWaitSoftmax, abort))
+          return false;
+        if (!mbar_wait(&sm.v_full[vs], (c.g / kVStages) & 1, fault, kFaultWaitTma, abort))
+          return false;
         tc_fence_after();
-        const uint32_t scol = bb ? kColS1 : kColS0;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint64_t ad = sdesc_sw128(smem_u32(sm.q[k >> 2]) + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(smem_u32(sm.k[st][k >> 2]) + (k & 3) * 32, 16, 1024);
-          mma_ss(tbase + scol, ad, bd, idS, k > 0 ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t bd = sdesc_sw128(smem_u32(sm.v[vs][0]) + kk * 2048, kTile, 1024);
+          mma_ts(tbase + kColO, tbase + b * 128 + kk * 8, bd, idO, (c.u > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&sm.s_full[bb]);
-        if (u >= 1) ok = pv(u - 1);
+        mma_commit(&sm.o_done[c.g & 1]);
+        mma_commit(&sm.v_empty[vs]);
+        return true;
+      };
+      Cursor qc, pc;
+      cursor_begin(a, qc);
+      cursor_begin(a, pc);
+      for (int j = 0; ok && j < 2 && qc.valid; ++j) {
+        ok = issue_qk(qc);
+        cursor_next(a, qc);
       }
-      if (ok) ok = pv(n - 1);
+      while (ok && pc.valid) {
+        if (qc.valid) {
+          ok = issue_qk(qc);
+          cursor_next(a, qc);
+          if (!ok) break;
+        }
+        ok = issue_pv(pc);
+        cursor_next(a, pc);
+      }
       // Nothing may be in flight when TMEM is released.
       mma_commit(&sm.drain);
       mbar_wait(&sm.drain, 0, fault, kFaultWaitMma);
@@ -279,169 +455,311 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   } else if (FP8 && warp >= R::kConvWarp0) {
     // ------------------------------------------------------------ E4M3 -> bf16
     const int ct = tid - R::kConvWarp0 * 32;
-    for (int u = 0; u < n; ++u) {
-      const int s8 = u % kF8Stages, st = u % kStages;
-      if (!mbar_wait(&sm.f8_full[s8], (u / kF8Stages) & 1, fault, kFaultWaitTma, abort)) break;
-      if (u >= kStages &&
-          !mbar_wait(&sm.kv_empty[st], ((u / kStages) - 1) & 1, fault, kFaultWaitMma, abort))
-        break;
-      convert_tile(sm.k8[s8], sm.k[st][0], ct);
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.k_full[st]);
-      convert_tile(sm.v8[s8], sm.v[st][0], ct);
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&sm.v_full[st]);
-        mbar_arrive(&sm.f8_empty[s8]);
+    int g = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; ok && i < a.num_items; i += gridDim.x) {
+      const Item it = item_at(a, i);
+      for (int u = 0; u < it.n; ++u, ++g) {
+        const int s8 = g % kF8Stages, ks = g % kKStages, vs = g % kVStages;
+        if (!mbar_wait(&sm.f8_full[s8], (g / kF8Stages) & 1, fault, kFaultWaitTma, abort) ||
+            (g >= kKStages && !mbar_wait(&sm.k_empty[ks], ((g / kKStages) - 1) & 1, fault,
+                                         kFaultWaitMma, abort))) {
+          ok = false;
+          break;
+        }
+        convert_tile(sm.k8[s8], sm.k[ks][0], ct);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.k_full[ks]);
+        if (g >= kVStages && !mbar_wait(&sm.v_empty[vs], ((g / kVStages) - 1) & 1, fault,
+                                        kFaultWaitMma, abort)) {
+          ok = false;
+          break;
+        }
+        convert_tile(sm.v8[s8], sm.v[vs][0], ct);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sm.v_full[vs]);
+          mbar_arrive(&sm.f8_empty[s8]);
+        }
       }
     }
   } else if (warp < R::kSoftmaxWarps) {
-    // ------------------------------------------------------------ softmax
+    // ------------------------------------------------------------ softmax + epilogue
     const int row = tid;  // TMEM lane
-    const int w = row / G, g = row - w * G;
-    const bool active = row < W * G && w < nw;
-    const long long pos = (long long)lk - lq + (t0 + w - seq_q0);
-    const uint32_t* mrow = a.member + (ubase * W + (active ? w : 0)) * a.words;
+    const int w = row / G, gh = row - w * G;
     const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
-    float m_ref = -INFINITY, l = 0.f;
-    uint32_t mword = 0;
-    bool pzero[2] = {false, false};
+    const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
     bool ok = true;
-    for (int u = 0; u < n; ++u) {
-      const int bb = u & 1;
-      if ((u & 31) == 0 && active) mword = __ldg(mrow + (u >> 5));
-      bool mem = active && ((mword >> (u & 31)) & 1u);
-      int lim = 127;
-      if (mem) {
-        const int blk = __ldg(ulist + u);
-        if (a.paged) {
-          const int page = __ldg(a.page_table + (size_t)b * a.max_pages + blk);
-          if (page < 0 || page >= a.num_pages) mem = false;
-        }
-        long long last = (long long)lk - 1;
-        if (a.causal && pos < last) last = pos;
-        last -= (long long)blk * kBlk;
-        if (last < 0) mem = false;
-        else if (last < 127) lim = (int)last;
-      }
-      ok = mbar_wait(&sm.s_full[bb], (u >> 1) & 1, fault, kFaultWaitMma, abort);
-      if (__any_sync(0xffffffffu, !ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const bool warp_mem = __any_sync(0xffffffffu, mem);
-      const uint32_t scol = lane_base + (bb ? kColS1 : kColS0);
-      const uint32_t pcol = lane_base + (bb ? kColP1 : kColP0);
-      float alpha = 1.f;
-      bool rescale = false;
-      if (warp_mem) {
-        // Pass 1: masked row max over the two 64-column halves of S.
-        float mx = -INFINITY;
+    int g = 0, rv = 0;  // blocks consumed, rendezvous count
+    // All four softmax warps meet here (bounded wait on an mbarrier).
+    auto rendezvous = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.ep_bar);
+      const bool r = mbar_wait(&sm.ep_bar, rv & 1, fault, kFaultWaitSoftmax, abort);
+      ++rv;
+      return !__any_sync(0xffffffffu, !r);
+    };
+    int i = blockIdx.x;
+    Item nxt = i < a.num_items ? item_at(a, i) : Item{};
+    for (; ok && i < a.num_items; i += gridDim.x) {
+      const Item it = nxt;
+      // The next item's metadata is fetched while this one runs.
+      if (i + (int)gridDim.x < a.num_items) nxt = item_at(a, i + gridDim.x);
+      if (it.t0 < 0) continue;
+      const int nw = min(W, it.seq_q0 + it.lq - it.t0);
+      const bool active = row < W * G && w < nw;
+      const size_t orow = (size_t)(it.t0 + w) * a.num_qo_heads + (size_t)it.h * G + gh;
+      const int nsplit = (it.n_union + a.pps - 1) / a.pps;  // splits holding blocks
+      if (it.n == 0) {
+        // A tile with no usable block at all: out = 0, lse = -inf.
+        if (it.split == 0 && it.n_union == 0 && active) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * 128);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float s[64];
-          tmem_ld64(scol + half * 64, s);
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (lim >= 127 || half * 64 + c <= lim) mx = fmaxf(mx, s[c]);
+          for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
+          if (a.lse != nullptr) a.lse[orow] = -INFINITY;
         }
+        continue;
+      }
+      const long long pos = (long long)it.lk - it.lq + (it.t0 + w - it.seq_q0);
+      const size_t unit = (size_t)it.h * a.max_tiles + it.tile;
+      const uint32_t* mrow = a.member + (unit * W + (active ? w : 0)) * a.words;
+      const int32_t* ulist = a.union_blocks + unit * a.cap + it.p_begin;
+      float m_ref = -INFINITY, l = 0.f;
+      // Per-block metadata for block u, fetched one block ahead.
+      uint32_t mword = active ? __ldg(mrow + (it.p_begin >> 5)) : 0u;
+      int nblk_id = __ldg(ulist);
+      int npage_ok = 1;
+      if (a.paged) {
+        const int pg = __ldg(a.page_table + (size_t)it.b * a.max_pages + nblk_id);
+        npage_ok = pg >= 0 && pg < a.num_pages;
+      }
+      for (int u = 0; u < it.n; ++u) {
+        const int gg = g + u, bb = gg % kSBuf;
+        const int upos = it.p_begin + u;  // position in the tile's union list
+        const int blk = nblk_id;
+        bool mem = active && ((mword >> (upos & 31)) & 1u) && npage_ok;
+        if (u + 1 < it.n) {
+          nblk_id = __ldg(ulist + u + 1);
+          if (a.paged) {
+            const int pg = __ldg(a.page_table + (size_t)it.b * a.max_pages + nblk_id);
+            npage_ok = pg >= 0 && pg < a.num_pages;
+          }
+          if (((upos + 1) & 31) == 0 && active) mword = __ldg(mrow + ((upos + 1) >> 5));
+        }
+        int lim = 127;
         if (mem) {
-          const float mrow_max = mx * a.scale_log2;
-          if (m_ref == -INFINITY || mrow_max > m_ref + kRescaleLog2) {
-            if (m_ref != -INFINITY) {
-              alpha = ex2(m_ref - mrow_max);
-              rescale = true;
-              l *= alpha;
-            }
-            m_ref = mrow_max;
-          }
+          long long last = (long long)it.lk - 1;
+          if (a.causal && pos < last) last = pos;
+          last -= (long long)blk * kBlk;
+          if (last < 0) mem = false;
+          else if (last < 127) lim = (int)last;
         }
-        // Pass 2: P = 2^(s*scale*log2e - m) as bf16 pairs (0 for masked keys
-        // and for rows whose token did not select this block). QK(u) having
-        // completed implies PV(u-2) completed, so P buffer bb is free.
-        const float neg_m = mem ? -m_ref : 0.f;
-        float sum = 0.f;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float s[64];
-          tmem_ld64(scol + half * 64, s);
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const int key = half * 64 + c;
-            float p0 = ex2(fmaf(s[c], a.scale_log2, neg_m));
-            float p1 = ex2(fmaf(s[c + 1], a.scale_log2, neg_m));
-            if (!mem || (lim < 127 && key > lim)) p0 = 0.f;
-            if (!mem || (lim < 127 && key + 1 > lim)) p1 = 0.f;
-            sum += p0 + p1;
-            pk[c >> 1] = pack_bf16x2(p0, p1);
-          }
-          tmem_st32(pcol + half * 32, pk);
-        }
-        if (mem) l += sum;
-        pzero[bb] = false;
-      } else if (!pzero[bb]) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = 0u;
-        tmem_st32(pcol, pk);
-        tmem_st32(pcol + 32, pk);
-        pzero[bb] = true;
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O must hold every PV up to u-1 before it is rescaled.
-        ok = mbar_wait(&sm.o_done[(u - 1) & 1], ((u - 1) >> 1) & 1, fault, kFaultWaitMma, abort);
+        // QK(gg) done: S is readable, and every PV up to gg-3 (the last user
+        // of this P buffer) has completed.
+        ok = mbar_wait(&sm.s_full[bb], (gg / kSBuf) & 1, fault, kFaultWaitMma, abort);
         if (__any_sync(0xffffffffu, !ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const bool warp_mem = __any_sync(0xffffffffu, mem);
+        const bool warp_masked = __any_sync(0xffffffffu, mem && lim < 127);
+        const uint32_t scol = lane_base + bb * 128;  // S_b, and P_b in its first 64 columns
+        float alpha = 1.f;
+        bool rescale = false;
+        if (warp_mem) {
+          float2 acc = make_float2(0.f, 0.f);
+          if (!FP8) {
+            float sv[128];
+            tmem_ld128(scol, sv);
+            if (warp_masked) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float o[64];
-          tmem_ld64(lane_base + kColO + half * 64, o);
-          uint32_t ow[64];
+              for (int c = 0; c < 128; ++c)
+                if (c > lim) sv[c] = -INFINITY;
+            }
+            const float mx = row_max128(sv);
+            update_max(mem, mx, a.scale_log2, m_ref, l, alpha, rescale);
+            // Non-member rows use -inf as their offset, so every P entry is 0.
+            const float neg_m = mem ? -m_ref : -INFINITY;
+            exp_pack_store<64>(sv, sc2, neg_m, acc, scol);
+            exp_pack_store<64>(sv + 64, sc2, neg_m, acc, scol + 32);
+          } else {
+            float mx = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 64; ++c) ow[c] = __float_as_uint(o[c] * alpha);
-          tmem_st64(lane_base + kColO + half * 64, ow);
+            for (int half = 0; half < 2; ++half) {
+              float sv[64];
+              tmem_ld64(scol + half * 64, sv);
+              if (warp_masked) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                  if (half * 64 + c > lim) sv[c] = -INFINITY;
+              }
+              mx = fmaxf(mx, row_max64(sv));
+            }
+            update_max(mem, mx, a.scale_log2, m_ref, l, alpha, rescale);
+            const float neg_m = mem ? -m_ref : -INFINITY;
+            // Columns 64..127 of S are read before P's second half (columns
+            // 32..63) is written over them.
+            float sh[64];
+            tmem_ld64(scol + 64, sh);
+            {
+              float sv[64];
+              tmem_ld64(scol, sv);
+              if (warp_masked) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                  if (c > lim) sv[c] = -INFINITY;
+              }
+              exp_pack_store<64>(sv, sc2, neg_m, acc, scol);
+            }
+            if (warp_masked) {
+#pragma unroll
+              for (int c = 0; c < 64; ++c)
+                if (64 + c > lim) sh[c] = -INFINITY;
+            }
+            exp_pack_store<64>(sh, sc2, neg_m, acc, scol + 32);
+          }
+          if (mem) l += acc.x + acc.y;
+        } else {
+          // QK(gg) overwrote this buffer: P must be rewritten (zeros) every block.
+          uint32_t pk[64];
+#pragma unroll
+          for (int c = 0; c < 64; ++c) pk[c] = 0u;
+          tmem_st64(scol, pk);
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          // O must hold every PV of this item up to gg-1 before it is rescaled.
+          ok = mbar_wait(&sm.o_done[(gg - 1) & 1], ((gg - 1) >> 1) & 1, fault, kFaultWaitMma,
+                         abort);
+          if (__any_sync(0xffffffffu, !ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float o[64];
+            tmem_ld64(lane_base + kColO + half * 64, o);
+            uint32_t ow[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) ow[c] = __float_as_uint(o[c] * alpha);
+            tmem_st64(lane_base + kColO + half * 64, ow);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_full[bb]);
+      }
+      if (!ok) break;
+      // ---------------------------------------------------- item epilogue
+      // PV(glast - 1) first: its completion implies PV(glast - 2)'s, which
+      // makes the wait on PV(glast)'s barrier phase unambiguous.
+      const int glast = g + it.n - 1;
+      if (glast >= 1)
+        ok = mbar_wait(&sm.o_done[(glast - 1) & 1], ((glast - 1) >> 1) & 1, fault, kFaultWaitMma,
+                       abort);
+      if (ok) ok = mbar_wait(&sm.o_done[glast & 1], (glast >> 1) & 1, fault, kFaultWaitMma, abort);
+      if (__any_sync(0xffffffffu, !ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const size_t part = (unit * a.splits + it.split) * a.rows_part;
+      const bool has = l > 0.f;
+      const float inv = has ? 1.f / l : 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float o[64];
+        tmem_ld64(lane_base + kColO + half * 64, o);
+        if (!active) continue;
+        if (nsplit == 1) {
+          uint4* dst =
+              reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * 128);
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            uint4 v4 = make_uint4(0u, 0u, 0u, 0u);
+            if (has)
+              v4 = make_uint4(pack_bf16x2(o[c] * inv, o[c + 1] * inv),
+                              pack_bf16x2(o[c + 2] * inv, o[c + 3] * inv),
+                              pack_bf16x2(o[c + 4] * inv, o[c + 5] * inv),
+                              pack_bf16x2(o[c + 6] * inv, o[c + 7] * inv));
+            dst[(half * 64 + c) >> 3] = v4;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(a.part_o + (part + row) * 128 + half * 64);
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) dst[c >> 2] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
         }
       }
+      // O has been read: the next item's first PV may overwrite it.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_full[bb]);
-    }
-    // ------------------------------------------------------------ epilogue
-    if (ok && n > 0) {
-      ok = mbar_wait(&sm.o_done[(n - 1) & 1], ((n - 1) >> 1) & 1, fault, kFaultWaitMma, abort);
-      ok = !__any_sync(0xffffffffu, !ok);
-    }
-    const bool has = ok && n > 0 && l > 0.f;
-    const size_t orow = (size_t)(t0 + w) * a.num_qo_heads + (size_t)h * G + g;
-    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * 128);
-    const float inv = has ? 1.f / l : 0.f;
-    if (ok && n > 0) tc_fence_after();
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float o[64];
-      if (ok && n > 0) tmem_ld64(lane_base + kColO + half * 64, o);
-      if (active && ok) {
-#pragma unroll
-        for (int c = 0; c < 64; c += 8) {
-          uint4 v4 = make_uint4(0u, 0u, 0u, 0u);
-          if (has)
-            v4 = make_uint4(pack_bf16x2(o[c] * inv, o[c + 1] * inv),
-                            pack_bf16x2(o[c + 2] * inv, o[c + 3] * inv),
-                            pack_bf16x2(o[c + 4] * inv, o[c + 5] * inv),
-                            pack_bf16x2(o[c + 6] * inv, o[c + 7] * inv));
-          dst[(half * 64 + c) >> 3] = v4;
-        }
+      if (lane == 0) mbar_arrive(&sm.o_free);
+      g += it.n;
+      if (nsplit == 1) {
+        if (active && a.lse != nullptr)
+          a.lse[orow] = has ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        continue;
       }
+      if (active) {
+        a.part_ml[(part + row) * 2] = m_ref;
+        a.part_ml[(part + row) * 2 + 1] = l;
+      }
+      // Last split of the tile to finish merges (atomic ticket, no waiting).
+      __threadfence();
+      if (!rendezvous()) {
+        ok = false;
+        break;
+      }
+      if (tid == 0) sm.ticket_last = atomicAdd(&a.tickets[unit], 1) == nsplit - 1;
+      if (!rendezvous()) {
+        ok = false;
+        break;
+      }
+      if (!sm.ticket_last) continue;
+      __threadfence();
+      if (active) {
+        const size_t p0 = unit * a.splits * a.rows_part;
+        float M = -INFINITY;
+        for (int sp = 0; sp < nsplit; ++sp)
+          M = fmaxf(M, __ldcg(a.part_ml + (p0 + (size_t)sp * a.rows_part + row) * 2));
+        float L = 0.f;
+        float acc[128];
+#pragma unroll
+        for (int c = 0; c < 128; ++c) acc[c] = 0.f;
+        if (M != -INFINITY) {
+          for (int sp = 0; sp < nsplit; ++sp) {
+            const size_t pr = p0 + (size_t)sp * a.rows_part + row;
+            const float ms = __ldcg(a.part_ml + pr * 2);
+            if (ms == -INFINITY) continue;
+            const float f = ex2(ms - M);
+            L += f * __ldcg(a.part_ml + pr * 2 + 1);
+            const float4* src = reinterpret_cast<const float4*>(a.part_o + pr * 128);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float4 ov = __ldcg(src + c);
+              acc[4 * c] += f * ov.x;
+              acc[4 * c + 1] += f * ov.y;
+              acc[4 * c + 2] += f * ov.z;
+              acc[4 * c + 3] += f * ov.w;
+            }
+          }
+        }
+        const float invL = L > 0.f ? 1.f / L : 0.f;
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * 128);
+#pragma unroll
+        for (int c = 0; c < 128; c += 8)
+          dst[c >> 3] = make_uint4(pack_bf16x2(acc[c] * invL, acc[c + 1] * invL),
+                                   pack_bf16x2(acc[c + 2] * invL, acc[c + 3] * invL),
+                                   pack_bf16x2(acc[c + 4] * invL, acc[c + 5] * invL),
+                                   pack_bf16x2(acc[c + 6] * invL, acc[c + 7] * invL));
+        if (a.lse != nullptr)
+          a.lse[orow] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+      }
+      if (tid == 0) a.tickets[unit] = 0;
     }
-    if (active && ok && a.lse != nullptr)
-      a.lse[orow] = has ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
   }
 
   tc_fence_before();
@@ -458,12 +776,26 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<FP8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.max_tiles, a.num_kv_heads);
+  const int grid = a.num_items < device_sm_count() ? a.num_items : device_sm_count();
+  if (grid <= 0) return cudaSuccess;
   prefill_kernel<FP8><<<grid, Roles<FP8>::kThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+int device_sm_count() {
+  static int cache[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   return a.kv_fp8 ? launch_t<true>(a, s) : launch_t<false>(a, s);

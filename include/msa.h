@@ -78,8 +78,11 @@ size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_he
  *   page_table   device int32 (B, max_pages) mapping batch-local block -> page,
  *                or NULL for flat K/V; requires seqused_k
  *   seqused_k    device int32 (B), valid keys per sequence (paged only)
- *   max_seqlen_q host bound on every Lq; the paged route with max_seqlen_q <= 4
- *                and G <= 16 runs the split-KV decode kernel
+ *   max_seqlen_q host bound on every Lq; with the tile count it decides how
+ *                the work is split: when there are fewer (tile, KV head) units
+ *                than the GPU has room for (decode-sized problems), each
+ *                tile's union list is split across several work items whose
+ *                partial results are merged on the device
  *   softmax_scale  <= 0 selects head_dim^-0.5
  *   out          device, (Tq, Hq, d), dtype of q; fully written
  *   lse          device float32 (Tq, Hq) or NULL
