@@ -49,7 +49,7 @@ constexpr int kMinSplitBlocks = 8;
 struct PrefillLayout {
   int W, max_tiles, cap, words;
   int splits, pps, rows_part, num_items;
-  size_t off_info, off_len, off_blocks, off_member, off_part_o, off_part_ml, off_tickets, total;
+  size_t off_info, off_len, off_blocks, off_member, off_part_o, off_part_ml, total;
 };
 
 PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk, int max_seqlen_q) {
@@ -98,8 +98,6 @@ PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk, 
   off += up256((size_t)units * L.splits * L.rows_part * 128 * sizeof(float));
   L.off_part_ml = off;
   off += up256((size_t)units * L.splits * L.rows_part * 2 * sizeof(float));
-  L.off_tickets = off;
-  off += up256((size_t)units * sizeof(int));
   L.total = off;
   return L;
 }
@@ -232,11 +230,6 @@ msa_status_t msa_sparse_attention_fwd(
   mark(0, stream);
   cudaError_t e = launch_build_union(u, stream);
   if (e != cudaSuccess) return MSA_CUDA_ERROR;
-  if (L.splits > 1) {
-    e = cudaMemsetAsync(ws + L.off_tickets, 0,
-                        (size_t)num_kv_heads * L.max_tiles * sizeof(int), stream);
-    if (e != cudaSuccess) return MSA_CUDA_ERROR;
-  }
   mark(1, stream);
 
   PrefillArgs a{};
@@ -280,7 +273,6 @@ msa_status_t msa_sparse_attention_fwd(
   a.num_items = L.num_items;
   a.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
   a.part_ml = reinterpret_cast<float*>(ws + L.off_part_ml);
-  a.tickets = reinterpret_cast<int*>(ws + L.off_tickets);
   e = launch_prefill(a, stream);
   mark(2, stream);
   return from_cuda(e);

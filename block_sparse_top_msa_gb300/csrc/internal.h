@@ -109,14 +109,13 @@ struct PrefillArgs {
   // by a persistent grid. splits == 1: each item owns its tile's whole union
   // and writes out/lse directly. splits > 1: item s takes union entries
   // [s*pps, (s+1)*pps); when a tile needs more than one split the items write
-  // fp32 partials (rows_part rows per item) and the last one to finish merges.
+  // fp32 partials (rows_part rows per item), combined by a second kernel.
   int splits;
   int pps;
   int rows_part;
   int num_items;
   float* part_o;        // (Hkv*max_tiles*splits, rows_part, 128)
   float* part_ml;       // (Hkv*max_tiles*splits, rows_part, 2)
-  int* tickets;         // (Hkv*max_tiles), zero before the launch
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 int device_sm_count();

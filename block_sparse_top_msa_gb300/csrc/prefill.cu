@@ -64,10 +64,8 @@ struct __align__(1024) PrefillSmem {
   uint64_t p_full[kSBuf];
   uint64_t o_done[2];
   uint64_t o_free;
-  uint64_t ep_bar;
   uint64_t drain;
   uint32_t tmem_base;
-  int ticket_last;
   int abort;
 };
 
@@ -282,7 +280,6 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) mbar_init(&sm.o_done[s], 1);
     mbar_init(&sm.o_free, 4);
-    mbar_init(&sm.ep_bar, 4);
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
     fence_mbar_init();
@@ -492,15 +489,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
     const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
     bool ok = true;
-    int g = 0, rv = 0;  // blocks consumed, rendezvous count
-    // All four softmax warps meet here (bounded wait on an mbarrier).
-    auto rendezvous = [&]() -> bool {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.ep_bar);
-      const bool r = mbar_wait(&sm.ep_bar, rv & 1, fault, kFaultWaitSoftmax, abort);
-      ++rv;
-      return !__any_sync(0xffffffffu, !r);
-    };
+    int g = 0;  // blocks consumed
     int i = blockIdx.x;
     Item nxt = i < a.num_items ? item_at(a, i) : Item{};
     for (; ok && i < a.num_items; i += gridDim.x) {
@@ -707,58 +696,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         a.part_ml[(part + row) * 2] = m_ref;
         a.part_ml[(part + row) * 2 + 1] = l;
       }
-      // Last split of the tile to finish merges (atomic ticket, no waiting).
-      __threadfence();
-      if (!rendezvous()) {
-        ok = false;
-        break;
-      }
-      if (tid == 0) sm.ticket_last = atomicAdd(&a.tickets[unit], 1) == nsplit - 1;
-      if (!rendezvous()) {
-        ok = false;
-        break;
-      }
-      if (!sm.ticket_last) continue;
-      __threadfence();
-      if (active) {
-        const size_t p0 = unit * a.splits * a.rows_part;
-        float M = -INFINITY;
-        for (int sp = 0; sp < nsplit; ++sp)
-          M = fmaxf(M, __ldcg(a.part_ml + (p0 + (size_t)sp * a.rows_part + row) * 2));
-        float L = 0.f;
-        float acc[128];
-#pragma unroll
-        for (int c = 0; c < 128; ++c) acc[c] = 0.f;
-        if (M != -INFINITY) {
-          for (int sp = 0; sp < nsplit; ++sp) {
-            const size_t pr = p0 + (size_t)sp * a.rows_part + row;
-            const float ms = __ldcg(a.part_ml + pr * 2);
-            if (ms == -INFINITY) continue;
-            const float f = ex2(ms - M);
-            L += f * __ldcg(a.part_ml + pr * 2 + 1);
-            const float4* src = reinterpret_cast<const float4*>(a.part_o + pr * 128);
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const float4 ov = __ldcg(src + c);
-              acc[4 * c] += f * ov.x;
-              acc[4 * c + 1] += f * ov.y;
-              acc[4 * c + 2] += f * ov.z;
-              acc[4 * c + 3] += f * ov.w;
-            }
-          }
-        }
-        const float invL = L > 0.f ? 1.f / L : 0.f;
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * 128);
-#pragma unroll
-        for (int c = 0; c < 128; c += 8)
-          dst[c >> 3] = make_uint4(pack_bf16x2(acc[c] * invL, acc[c + 1] * invL),
-                                   pack_bf16x2(acc[c + 2] * invL, acc[c + 3] * invL),
-                                   pack_bf16x2(acc[c + 4] * invL, acc[c + 5] * invL),
-                                   pack_bf16x2(acc[c + 6] * invL, acc[c + 7] * invL));
-        if (a.lse != nullptr)
-          a.lse[orow] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-      }
-      if (tid == 0) a.tickets[unit] = 0;
+      // The tile's splits are combined by merge_splits_kernel after this launch.
     }
   }
 
@@ -770,6 +708,56 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   }
 }
 
+
+// Combines the fp32 partials of tiles whose union was split across several
+// work items: for each (tile, KV head) unit and active row, with
+// M = max_s m_s, L = sum_s 2^(m_s - M) l_s, out = sum_s 2^(m_s - M) O_s / L and
+// lse = (M + log2 L) ln 2 (m in log2 units of the scaled logits). One warp per
+// (unit, row); each lane owns four of the 128 dims.
+__global__ void __launch_bounds__(256) merge_splits_kernel(const __grid_constant__ PrefillArgs a) {
+  const int warp_global = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  const int units = a.num_kv_heads * a.max_tiles;
+  if (warp_global >= units * a.rows_part) return;
+  const int unit = warp_global / a.rows_part, row = warp_global - unit * a.rows_part;
+  const int h = unit / a.max_tiles, tile = unit - h * a.max_tiles;
+  const int t0 = __ldg(a.tile_info + 2 * tile);
+  if (t0 < 0) return;
+  const int n_union = __ldg(a.union_len + unit);
+  const int nsplit = (n_union + a.pps - 1) / a.pps;
+  if (nsplit <= 1) return;  // written directly by the attention kernel
+  const int G = a.num_qo_heads / a.num_kv_heads;
+  const int b = __ldg(a.tile_info + 2 * tile + 1);
+  const int nw = min(a.tile_tokens, __ldg(a.cu_q + b + 1) - t0);
+  const int w = row / G, gh = row - w * G;
+  if (row >= a.tile_tokens * G || w >= nw) return;
+  const size_t p0 = (size_t)unit * a.splits * a.rows_part + row;
+  float M = -INFINITY;
+  for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldg(a.part_ml + (p0 + (size_t)sp * a.rows_part) * 2));
+  float L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const size_t pr = p0 + (size_t)sp * a.rows_part;
+      const float ms = __ldg(a.part_ml + pr * 2);
+      if (ms == -INFINITY) continue;
+      const float f = ex2(ms - M);
+      L += f * __ldg(a.part_ml + pr * 2 + 1);
+      const float4 ov = __ldg(reinterpret_cast<const float4*>(a.part_o + pr * 128) + lane);
+      acc.x += f * ov.x;
+      acc.y += f * ov.y;
+      acc.z += f * ov.z;
+      acc.w += f * ov.w;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const size_t orow = (size_t)(t0 + w) * a.num_qo_heads + (size_t)h * G + gh;
+  uint2* dst = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * 128) + lane;
+  *dst = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (lane == 0 && a.lse != nullptr)
+    a.lse[orow] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+}
+
 template <bool FP8>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   const size_t smem = sizeof(PrefillSmem<FP8>) + 1024;
@@ -779,6 +767,10 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   const int grid = a.num_items < device_sm_count() ? a.num_items : device_sm_count();
   if (grid <= 0) return cudaSuccess;
   prefill_kernel<FP8><<<grid, Roles<FP8>::kThreads, smem, s>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.splits <= 1) return e;
+  const long long warps = (long long)a.num_kv_heads * a.max_tiles * a.rows_part;
+  merge_splits_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
 

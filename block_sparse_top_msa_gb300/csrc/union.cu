@@ -135,12 +135,130 @@ __global__ void __launch_bounds__(kUnionThreads)
   }
 }
 
+// Fast path for W * topk <= 1024: one key per thread (blockDim.x = P, a power
+// of two >= 32), bitonic sort in registers with warp shuffles for strides
+// below 32 and shared memory for the larger ones, ballot-based compaction.
+__global__ void __launch_bounds__(1024) build_union_small_kernel(UnionArgs a) {
+  extern __shared__ int smem_i[];
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, wid = tid >> 5;
+  const int tile = blockIdx.x, h = blockIdx.y;
+  int* scratch = smem_i;             // nt + 2 (tile lookup), then nt (sort exchange)
+  int* ulist = scratch + nt + 2;     // cap
+  uint32_t* mem = reinterpret_cast<uint32_t*>(ulist + a.cap);  // W * words
+  __shared__ int s_warp[32];
+  __shared__ int s_ulen;
+
+  int b = 0, t0 = 0;
+  const bool live = locate_tile(a.cu_q, a.batch, a.tile_tokens, tile, scratch, &b, &t0);
+  const size_t base = (size_t)h * a.max_tiles + tile;
+  if (!live) {
+    if (tid == 0) a.union_len[base] = 0;
+    for (int j = tid; j < a.cap; j += nt) a.union_blocks[base * a.cap + j] = -1;
+    for (int j = tid; j < a.tile_tokens * a.words; j += nt)
+      a.member[base * a.tile_tokens * a.words + j] = 0u;
+    if (a.tile_info != nullptr && h == 0 && tid < 2) a.tile_info[2 * tile + tid] = -1;
+    return;
+  }
+  const int end = a.cu_q[b + 1];
+  const int lq = end - a.cu_q[b];
+  const int lk = a.seqused_k ? a.seqused_k[b] : a.cu_k[b + 1] - a.cu_k[b];
+  int nblk = (lk + kBlk - 1) / kBlk;
+  if (a.seqused_k && nblk > a.max_pages) nblk = a.max_pages;
+  const int nw = min(a.tile_tokens, end - t0);
+  const int n = a.tile_tokens * a.topk;
+
+  // This thread's id (usable ids only; the rest sort to the end).
+  int key = INT_MAX;
+  int my_id = -1, my_w = 0;
+  if (tid < n) {
+    my_w = tid / a.topk;
+    if (my_w < nw) {
+      const int id = a.q2k[((size_t)h * a.total_q + t0 + my_w) * a.topk + (tid % a.topk)];
+      const long long pos = (long long)lk - lq + (t0 + my_w - a.cu_q[b]);
+      if (id >= 0 && id < nblk && (!a.causal || (long long)id * kBlk <= pos)) {
+        key = id;
+        my_id = id;
+      }
+    }
+  }
+  for (int j = tid; j < a.tile_tokens * a.words; j += nt) mem[j] = 0u;
+  int* xchg = scratch;  // reused: the tile lookup is done
+  __syncthreads();
+  for (int k = 2; k <= nt; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      int other;
+      if (j >= 32) {
+        xchg[tid] = key;
+        __syncthreads();
+        other = xchg[tid ^ j];
+        __syncthreads();
+      } else {
+        other = __shfl_xor_sync(0xffffffffu, key, j);
+      }
+      const bool up = (tid & k) == 0, lower = (tid & j) == 0;
+      key = (lower == up) ? min(key, other) : max(key, other);
+    }
+  }
+  // First occurrence of each distinct usable id.
+  xchg[tid] = key;
+  __syncthreads();
+  const int prev = tid > 0 ? xchg[tid - 1] : INT_MIN;
+  const bool flag = key != INT_MAX && key != prev;
+  const unsigned ball = __ballot_sync(0xffffffffu, flag);
+  if (lane == 0) s_warp[wid] = __popc(ball);
+  __syncthreads();
+  if (wid == 0) {
+    const int nwarps = nt >> 5;
+    int v = lane < nwarps ? s_warp[lane] : 0;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += u;
+    }
+    if (lane < nwarps) s_warp[lane] = v;  // inclusive
+    if (lane == 31) s_ulen = v;
+  }
+  __syncthreads();
+  const int before = (wid > 0 ? s_warp[wid - 1] : 0) + __popc(ball & ((1u << lane) - 1u));
+  if (flag) ulist[before] = key;
+  const int ulen = s_ulen;
+  __syncthreads();
+  // Membership bits: binary search of this thread's original id.
+  if (my_id >= 0) {
+    int lo = 0, hi = ulen - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (ulist[mid] < my_id) lo = mid + 1; else hi = mid;
+    }
+    atomicOr(&mem[my_w * a.words + (lo >> 5)], 1u << (lo & 31));
+  }
+  __syncthreads();
+  if (tid == 0) a.union_len[base] = ulen;
+  for (int j = tid; j < a.cap; j += nt) a.union_blocks[base * a.cap + j] = j < ulen ? ulist[j] : -1;
+  for (int j = tid; j < a.tile_tokens * a.words; j += nt)
+    a.member[base * a.tile_tokens * a.words + j] = mem[j];
+  if (a.tile_info != nullptr && h == 0 && tid == 0) {
+    a.tile_info[2 * tile] = t0;
+    a.tile_info[2 * tile + 1] = b;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_build_union(const UnionArgs& a, cudaStream_t s) {
   const int n = a.tile_tokens * a.topk;
   int P = 1;
   while (P < n) P <<= 1;
+  if (P <= 1024) {
+    const int nt = P < 32 ? 32 : P;
+    const size_t smem =
+        sizeof(int) * ((size_t)nt + 2 + a.cap + (size_t)a.tile_tokens * a.words);
+    cudaError_t e = cudaFuncSetAttribute(build_union_small_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.max_tiles, a.num_kv_heads);
+    build_union_small_kernel<<<grid, nt, smem, s>>>(a);
+    return cudaGetLastError();
+  }
   const size_t smem =
       sizeof(int) * ((size_t)kUnionThreads + 2 + P + a.cap + (size_t)a.tile_tokens * a.words);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;

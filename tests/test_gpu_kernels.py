@@ -67,7 +67,8 @@ def _oracle(inp, causal=True, scale=None, rows=None):
 # ---------------------------------------------------------------- union metadata
 @pytest.mark.parametrize("W,topk,lens", [(16, 16, [300, 45, 1000]), (32, 4, [1024]),
                                          (1, 3, [77, 300]), (128, 8, [600, 129]),
-                                         (10, 5, [333])])
+                                         (10, 5, [333]), (128, 16, [2000, 129]),
+                                         (64, 40, [3000])])
 def test_union_bit_exact(msa, W, topk, lens):
     g = torch.Generator().manual_seed(W * 7 + topk)
     hkv = 3
@@ -137,6 +138,7 @@ PREFILL_CASES = [
     ("e4m3_mha_lq_lt_lk", [100], [900], 2, 2, 7, "e4m3", False),
     ("topk1", [300], [300], 8, 1, 1, "bf16", False),
     ("topk64", [1200], [1200], 8, 1, 64, "bf16", False),
+    ("mha_topk16_wide_union", [700, 260], [700, 260], 2, 2, 16, "bf16", True),
 ]
 
 
