@@ -330,7 +330,7 @@ def bench_prefill(msa, args, device, world, rank):
 
 
 # ---------------------------------------------------------------- secondary: paged decode
-DECODE_PROFILE_SPEC = workloads.DecodeSpec("paged_decode_b32_U[8192,32768]_h64kv4_top16", 32,
+DECODE_PROFILE_SPEC = workloads.DecodeSpec("paged_decode_b64_U[8192,32768]_h64kv4_top16", 64,
                                            (8192, 32768), 64, 4, 16)
 
 
@@ -509,7 +509,7 @@ def main():
     ap.add_argument("--profile-small", action="store_true",
                     help="profiling case: prefill only, 1 x 8192 tokens, 64/8 heads, top-16")
     ap.add_argument("--profile-decode", type=int, default=0, metavar="SQ",
-                    help="profiling case: paged decode only, 32 requests, seqlen_q SQ")
+                    help="profiling case: paged decode only, 64 requests, seqlen_q SQ")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -54,7 +54,10 @@ struct PrefillLayout {
 
 PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk, int max_seqlen_q) {
   PrefillLayout L{};
+  // Tiles never span sequences, so capping W at the longest query run changes
+  // no tile; it only shrinks the union arrays and the Q tile of short runs.
   L.W = tile_tokens_for(hq, hkv);
+  if (max_seqlen_q >= 1 && max_seqlen_q < L.W) L.W = max_seqlen_q;
   L.max_tiles = (total_q + L.W - 1) / L.W + batch;
   L.cap = L.W * topk;
   L.words = (L.cap + 31) / 32;

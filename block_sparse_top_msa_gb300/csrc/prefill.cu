@@ -43,11 +43,18 @@ constexpr float kRescaleLog2 = 8.0f;
 // has read S_b), O at 384.
 constexpr uint32_t kColO = 384;
 
-template <bool FP8>
+// STREAM: layout for memory-bound launches (decode-sized problems split into
+// many short items, at most 64 real Q rows). Their two Q slots share one
+// 32 KiB region, slot j starting j * rows * 128 bytes in: each slot's real
+// rows stay clear of the other's, and the rows an M=128 MMA reads past them
+// (other slots, or the K ring) only feed S rows no token owns. That leaves
+// room for a four-deep V ring. Otherwise two separate Q buffers.
+template <bool FP8, bool STREAM = false>
 struct __align__(1024) PrefillSmem {
-  static constexpr int kQBuf = FP8 ? 1 : 2;     // Q tiles of consecutive work items
-  static constexpr int kVStages = FP8 ? 2 : 3;  // V ring (a slot frees when its PV completes)
-  uint8_t q[kQBuf][2][kTile];
+  static constexpr int kQBuf = FP8 ? 1 : 2;                       // Q tiles of consecutive items
+  static constexpr int kQRegions = STREAM ? 1 : kQBuf;
+  static constexpr int kVStages = FP8 ? 2 : (STREAM ? 4 : 3);     // V ring (frees when its PV completes)
+  uint8_t q[kQRegions][2][kTile];
   uint8_t k[kKStages][2][kTile];
   uint8_t v[kVStages][2][kTile];
   uint8_t k8[FP8 ? kF8Stages : 1][FP8 ? kTile : 16];
@@ -241,11 +248,11 @@ MSA_DEV void cursor_begin(const PrefillArgs& a, Cursor& c) {
   cursor_next(a, c);
 }
 
-template <bool FP8>
+template <bool FP8, bool STREAM>
 __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a) {
   using R = Roles<FP8>;
-  using Smem = PrefillSmem<FP8>;
+  using Smem = PrefillSmem<FP8, STREAM>;
   constexpr int kQBuf = Smem::kQBuf;
   constexpr int kVStages = Smem::kVStages;
   extern __shared__ uint8_t smem_raw[];
@@ -256,6 +263,11 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.num_qo_heads / a.num_kv_heads;
   const int W = a.tile_tokens;
+  // Shared-memory address of half c of Q slot qb.
+  auto q_addr = [&](int qb, int c) -> uint8_t* {
+    if (STREAM) return &sm.q[0][c][0] + (size_t)qb * (W * G) * 128;
+    return &sm.q[qb][c][0];
+  };
 
   if (tid == 0) {
     for (int s = 0; s < kQBuf; ++s) {
@@ -317,7 +329,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         }
         mbar_expect_tx(&sm.q_full[qb], 2u * 128u * (uint32_t)(G * W));
         for (int c = 0; c < 2; ++c)
-          tma_load_3d(sm.q[qb][c], &a.tmap_q, &sm.q_full[qb], c * 64, it.h * G, it.t0);
+          tma_load_3d(q_addr(qb, c), &a.tmap_q, &sm.q_full[qb], c * 64, it.h * G, it.t0);
         const int32_t* ulist =
             a.union_blocks + ((size_t)it.h * a.max_tiles + it.tile) * a.cap + it.p_begin;
         for (int u = 0; u < it.n; ++u, ++g) {
@@ -400,7 +412,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc_sw128(smem_u32(sm.q[qb][kk >> 2]) + (kk & 3) * 32, 16, 1024);
+          const uint64_t ad = sdesc_sw128(smem_u32(q_addr(qb, kk >> 2)) + (kk & 3) * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(smem_u32(sm.k[ks][kk >> 2]) + (kk & 3) * 32, 16, 1024);
           mma_ss(tbase + b * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
         }
@@ -758,15 +770,15 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const __grid_constant
     a.lse[orow] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
-template <bool FP8>
+template <bool FP8, bool STREAM>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
-  const size_t smem = sizeof(PrefillSmem<FP8>) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<FP8>,
+  const size_t smem = sizeof(PrefillSmem<FP8, STREAM>) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<FP8, STREAM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = a.num_items < device_sm_count() ? a.num_items : device_sm_count();
   if (grid <= 0) return cudaSuccess;
-  prefill_kernel<FP8><<<grid, Roles<FP8>::kThreads, smem, s>>>(a);
+  prefill_kernel<FP8, STREAM><<<grid, Roles<FP8>::kThreads, smem, s>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.splits <= 1) return e;
   const long long warps = (long long)a.num_kv_heads * a.max_tiles * a.rows_part;
@@ -790,7 +802,12 @@ int device_sm_count() {
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
-  return a.kv_fp8 ? launch_t<true>(a, s) : launch_t<false>(a, s);
+  if (a.kv_fp8) return launch_t<true, false>(a, s);
+  // Split launches are the memory-bound, decode-sized ones; their Q slots
+  // share a region when a tile has at most 64 rows (whole 8-row groups).
+  const int rows = a.tile_tokens * (a.num_qo_heads / a.num_kv_heads);
+  const bool stream = a.splits > 1 && rows <= 64 && rows % 8 == 0;
+  return stream ? launch_t<false, true>(a, s) : launch_t<false, false>(a, s);
 }
 
 }  // namespace msa

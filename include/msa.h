@@ -174,7 +174,9 @@ msa_status_t msa_build_union(const int32_t* q2k_indices, int topk, const int32_t
                              int max_tiles, int32_t* union_len, int32_t* union_blocks,
                              uint32_t* member, int32_t* tile_info, cudaStream_t stream);
 
-/* Tokens per query tile the forward uses for Hq/Hkv: floor(128 / G), at least 1. */
+/* Tokens per query tile for Hq/Hkv: floor(128 / G), at least 1. The forward
+ * uses min(this, max_seqlen_q), which forms the same tiles (tiles never span
+ * sequences). */
 int msa_union_tile_tokens(int num_qo_heads, int num_kv_heads);
 
 /*
