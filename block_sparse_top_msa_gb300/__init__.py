@@ -77,6 +77,8 @@ def lib():
         L.msa_sparse_decode_noalloc_scratch_limit.argtypes = []
         L.msa_set_timing_events.restype = i32
         L.msa_set_timing_events.argtypes = [C.POINTER(C.c_void_p), i32]
+        L.msa_selftest_wait_timeout.restype = i32
+        L.msa_selftest_wait_timeout.argtypes = [C.c_uint, vp]
         L.msa_read_device_fault.restype = i32
         L.msa_read_device_fault.argtypes = [C.POINTER(C.c_uint), vp]
         _lib = L
@@ -294,3 +296,9 @@ def msa_sparse_decode_noalloc(q, k, v, q2k_indices, cu_seqlens_q, page_table, se
         _p(lse), _stream(stream))
     _check("msa_sparse_decode_noalloc", st)
     return (out, lse) if lse is not None else out
+
+
+def msa_selftest_wait_timeout(timeout_us, stream=None):
+    """Run the bounded-wait self-test kernel (see include/msa.h)."""
+    _check("msa_selftest_wait_timeout", lib().msa_selftest_wait_timeout(int(timeout_us),
+                                                                        _stream(stream)))

@@ -41,14 +41,14 @@ int tile_tokens_for(int hq, int hkv) {
   return G >= 128 ? 1 : 128 / G;
 }
 
-// Work items the persistent attention kernel aims for (about 8 per SM of a
-// 152-SM GB300); fewer (tile, KV head) units than this split their union lists.
-constexpr int kTargetItems = 8 * 152;
-constexpr int kMinSplitBlocks = 8;
+// Work planning for the persistent attention kernel assumes a 152-SM GB300
+// (device-independent, so the workspace size query needs no device).
+constexpr int kPlanSMs = 152;
+constexpr int kMinSplitBlocks = 4;
 
 struct PrefillLayout {
   int W, max_tiles, cap, words;
-  int splits, pps, rows_part, num_items;
+  int whole_units, tail_units, splits, pps, rows_part, num_items;
   size_t off_info, off_len, off_blocks, off_member, off_part_o, off_part_ml, total;
 };
 
@@ -57,37 +57,51 @@ PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk, 
   // Tiles never span sequences, so capping W at the longest query run changes
   // no tile; it only shrinks the union arrays and the Q tile of short runs.
   L.W = tile_tokens_for(hq, hkv);
-  if (max_seqlen_q >= 1 && max_seqlen_q < L.W) L.W = max_seqlen_q;
-  L.max_tiles = (total_q + L.W - 1) / L.W + batch;
+  const int sq = max_seqlen_q < 1 ? 1 : max_seqlen_q;
+  if (sq < L.W) L.W = sq;
+  // Tile count bound: sum_b ceil(Lq_b / W) <= ceil(total_q / W) + batch, a tile
+  // has at least one token, and with W >= every Lq a sequence has one tile.
+  long long mt = ((long long)total_q + L.W - 1) / L.W + batch;
+  if (total_q > 0 && mt > total_q) mt = total_q;
+  if (L.W >= sq && mt > batch) mt = batch;
+  if (mt < 1) mt = 1;
+  L.max_tiles = (int)mt;
   L.cap = L.W * topk;
   L.words = (L.cap + 31) / 32;
   const int G = hq / hkv;
   const long long units = (long long)hkv * L.max_tiles;
-  const int sq = max_seqlen_q < 1 ? 1 : max_seqlen_q;
   // Longest union a tile can have: its tokens' selections, at most cap.
-  const int bound = (int)((long long)(sq < L.W ? sq : L.W) * topk < L.cap
-                              ? (long long)(sq < L.W ? sq : L.W) * topk
-                              : L.cap);
+  const long long bound_ll = (long long)L.W * topk;
+  const int bound = (int)(bound_ll < L.cap ? bound_ll : L.cap);
+  // Whole units fill complete rounds of the SMs; the remainder ("tail") is
+  // split so the last round is spread over all SMs.
+  L.whole_units = (int)units;
+  L.tail_units = 0;
   L.splits = 1;
   L.pps = L.cap;
-  if (units < kTargetItems) {
-    int S = (int)((kTargetItems + units - 1) / units);
+  const long long rem = units % kPlanSMs;
+  if (rem > 0) {
+    int S = (int)((kPlanSMs + rem - 1) / rem);
     if (S > bound) S = bound;
     if (S > 1) {
-      // At least kMinSplitBlocks blocks per item, so per-item work (Q load,
-      // partial write, merge) stays small next to the K/V stream.
-      L.pps = (bound + S - 1) / S;
-      if (L.pps < kMinSplitBlocks) L.pps = kMinSplitBlocks;
-      L.splits = (bound + L.pps - 1) / L.pps;
-      if (L.splits == 1) L.pps = L.cap;
+      int pps = (bound + S - 1) / S;
+      if (pps < kMinSplitBlocks) pps = kMinSplitBlocks;
+      S = (bound + pps - 1) / pps;
+      if (S > 1) {
+        L.splits = S;
+        L.pps = pps;
+        L.tail_units = (int)rem;
+        L.whole_units = (int)(units - rem);
+      }
     }
   }
   L.rows_part = 0;
-  if (L.splits > 1) {
-    const int rows = (sq < L.W ? sq : L.W) * G;
+  if (L.tail_units > 0) {
+    const int rows = L.W * G;
     L.rows_part = rows >= 128 ? 128 : ((rows + 15) / 16) * 16;
   }
-  L.num_items = (int)(units * L.splits);
+  L.num_items = L.whole_units + L.tail_units * L.splits;
+  const size_t parts = (size_t)L.tail_units * L.splits;
   size_t off = 0;
   L.off_info = off;
   off += up256((size_t)L.max_tiles * 2 * sizeof(int32_t));
@@ -98,9 +112,9 @@ PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk, 
   L.off_member = off;
   off += up256((size_t)units * L.W * L.words * sizeof(uint32_t));
   L.off_part_o = off;
-  off += up256((size_t)units * L.splits * L.rows_part * 128 * sizeof(float));
+  off += up256(parts * L.rows_part * 128 * sizeof(float));
   L.off_part_ml = off;
-  off += up256((size_t)units * L.splits * L.rows_part * 2 * sizeof(float));
+  off += up256(parts * L.rows_part * 2 * sizeof(float));
   L.total = off;
   return L;
 }
@@ -270,6 +284,8 @@ msa_status_t msa_sparse_attention_fwd(
   a.tile_info = u.tile_info;
   a.out = out;
   a.lse = lse;
+  a.whole_units = L.whole_units;
+  a.tail_units = L.tail_units;
   a.splits = L.splits;
   a.pps = L.pps;
   a.rows_part = L.rows_part;

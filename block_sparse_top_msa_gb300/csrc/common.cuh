@@ -70,8 +70,8 @@ MSA_DEV bool mbar_test(uint64_t* bar, uint32_t parity) {
 // Waits until the phase with the given parity has completed. Gives up after
 // kWaitLimitNs (or as soon as *abort is set by another warp of the CTA),
 // recording `code` in the fault word; returns false in that case.
-MSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* fault, unsigned code,
-                       volatile int* abort = nullptr) {
+MSA_DEV bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned* fault, unsigned code,
+                           unsigned long long limit_ns, volatile int* abort = nullptr) {
   if (mbar_test(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
@@ -79,12 +79,16 @@ MSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* fault, unsigned
     for (int i = 0; i < 64; ++i)
       if (mbar_test(bar, parity)) return true;
     if (abort != nullptr && *abort) return false;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       if (fault) atomicOr(fault, code);
       if (abort) *abort = 1;
       return false;
     }
   }
+}
+MSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* fault, unsigned code,
+                       volatile int* abort = nullptr) {
+  return mbar_wait_for(bar, parity, fault, code, kWaitLimitNs, abort);
 }
 
 // ---------------------------------------------------------------- TMA
@@ -237,5 +241,16 @@ MSA_DEV uint32_t sw128_offset(uint32_t row, uint32_t c16) {
 }
 
 MSA_DEV int elect_lane0() { return (threadIdx.x & 31) == 0; }
+
+// Programmatic dependent launch: block until the grid launched before this
+// one on the stream has completed and its writes are visible. A no-op when
+// the kernel was launched without the programmatic-serialization attribute.
+MSA_DEV void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream (launched with programmatic
+// serialization) start its prologue now; it still waits for this grid's
+// completion before reading its results.
+MSA_DEV void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 }  // namespace msa

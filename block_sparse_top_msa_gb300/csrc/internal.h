@@ -105,17 +105,21 @@ struct PrefillArgs {
   const int32_t* tile_info;
   void* out;
   float* lse;
-  // Work items (query tile, KV head, split of the tile's union list), walked
-  // by a persistent grid. splits == 1: each item owns its tile's whole union
-  // and writes out/lse directly. splits > 1: item s takes union entries
-  // [s*pps, (s+1)*pps); when a tile needs more than one split the items write
-  // fp32 partials (rows_part rows per item), combined by a second kernel.
+  // Work items, walked by a persistent grid. Units are (query tile, KV head)
+  // pairs, heaviest first. The first whole_units units are one item each and
+  // write out/lse directly. Each remaining ("tail") unit is split into
+  // `splits` items, item s taking union entries [s*pps, (s+1)*pps); a tail
+  // unit whose union needs more than one split writes fp32 partials
+  // (rows_part rows per item), combined by a second kernel.
+  // Splitting only the tail evens out the last round of work across the SMs.
+  int whole_units;
+  int tail_units;
   int splits;
   int pps;
   int rows_part;
   int num_items;
-  float* part_o;        // (Hkv*max_tiles*splits, rows_part, 128)
-  float* part_ml;       // (Hkv*max_tiles*splits, rows_part, 2)
+  float* part_o;        // (tail_units*splits, rows_part, 128)
+  float* part_ml;       // (tail_units*splits, rows_part, 2)
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 int device_sm_count();

@@ -32,7 +32,7 @@
 namespace msa {
 namespace {
 
-constexpr int kKStages = 2;     // K ring (a slot frees when its QK completes)
+constexpr int kKStagesMax = 3;  // K ring (a slot frees when its QK completes)
 constexpr int kF8Stages = 2;    // E4M3 staging ring (K and V bytes of one block)
 constexpr int kSBuf = 3;        // S/P buffers in TMEM: QK runs two blocks ahead of PV
 constexpr int kTile = 16384;    // bytes of one 128-row x 128-byte swizzled tile
@@ -53,7 +53,8 @@ template <bool FP8, bool STREAM = false>
 struct __align__(1024) PrefillSmem {
   static constexpr int kQBuf = FP8 ? 1 : 2;                       // Q tiles of consecutive items
   static constexpr int kQRegions = STREAM ? 1 : kQBuf;
-  static constexpr int kVStages = FP8 ? 2 : (STREAM ? 4 : 3);     // V ring (frees when its PV completes)
+  static constexpr int kKStages = STREAM ? 3 : 2;                 // K ring (frees when its QK completes)
+  static constexpr int kVStages = FP8 ? 2 : 3;                    // V ring (frees when its PV completes)
   uint8_t q[kQRegions][2][kTile];
   uint8_t k[kKStages][2][kTile];
   uint8_t v[kVStages][2][kTile];
@@ -61,8 +62,8 @@ struct __align__(1024) PrefillSmem {
   uint8_t v8[FP8 ? kF8Stages : 1][FP8 ? kTile : 16];
   uint64_t q_full[kQBuf];
   uint64_t q_empty[kQBuf];
-  uint64_t k_full[kKStages];
-  uint64_t k_empty[kKStages];
+  uint64_t k_full[kKStagesMax];
+  uint64_t k_empty[kKStagesMax];
   uint64_t v_full[kVStages];
   uint64_t v_empty[kVStages];
   uint64_t f8_full[kF8Stages];
@@ -182,26 +183,35 @@ MSA_DEV void convert_tile(const uint8_t* src, uint8_t* dst_half0, int t) {
 // tile's union list. Every role derives the same items in the same order.
 struct Item {
   int tile, h, split, t0, b, n_union, p_begin, n;
+  int tail;                 // index among the split (tail) units, or -1 for a whole unit
   int seq_q0, lq, lk, kv0;  // the tile's sequence (valid when t0 >= 0)
 };
 
 MSA_DEV Item item_at(const PrefillArgs& a, int i) {
-  const int per_tile = a.num_kv_heads * a.splits;
-  const int tile_idx = i / per_tile;
-  const int rem = i - tile_idx * per_tile;
   Item it;
+  int unit;
+  if (i < a.whole_units) {
+    unit = i;
+    it.split = 0;
+    it.tail = -1;
+  } else {
+    const int j = i - a.whole_units;
+    it.tail = j / a.splits;
+    it.split = j - it.tail * a.splits;
+    unit = a.whole_units + it.tail;
+  }
+  const int tile_idx = unit / a.num_kv_heads;
+  it.h = unit - tile_idx * a.num_kv_heads;
   it.tile = a.max_tiles - 1 - tile_idx;  // later (heavier) tiles first
-  it.h = rem / a.splits;
-  it.split = rem - it.h * a.splits;
   it.t0 = __ldg(a.tile_info + 2 * it.tile);
   it.b = __ldg(a.tile_info + 2 * it.tile + 1);
-  it.p_begin = it.split * a.pps;
+  it.p_begin = it.tail < 0 ? 0 : it.split * a.pps;
   it.n_union = 0;
   it.n = 0;
   it.seq_q0 = it.lq = it.lk = it.kv0 = 0;
   if (it.t0 >= 0) {
     it.n_union = __ldg(a.union_len + (size_t)it.h * a.max_tiles + it.tile);
-    it.n = max(0, min(it.n_union, it.p_begin + a.pps) - it.p_begin);
+    it.n = it.tail < 0 ? it.n_union : max(0, min(it.n_union, it.p_begin + a.pps) - it.p_begin);
     it.seq_q0 = __ldg(a.cu_q + it.b);
     it.lq = __ldg(a.cu_q + it.b + 1) - it.seq_q0;
     if (a.paged) {
@@ -254,6 +264,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   using R = Roles<FP8>;
   using Smem = PrefillSmem<FP8, STREAM>;
   constexpr int kQBuf = Smem::kQBuf;
+  constexpr int kKStages = Smem::kKStages;
   constexpr int kVStages = Smem::kVStages;
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -304,6 +315,10 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
+  // Everything above overlaps the tail of the union-metadata kernel; its
+  // results are read only after this wait (programmatic dependent launch).
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   if (warp == R::kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -512,7 +527,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       const int nw = min(W, it.seq_q0 + it.lq - it.t0);
       const bool active = row < W * G && w < nw;
       const size_t orow = (size_t)(it.t0 + w) * a.num_qo_heads + (size_t)it.h * G + gh;
-      const int nsplit = (it.n_union + a.pps - 1) / a.pps;  // splits holding blocks
+      // Items holding blocks of this unit (a whole unit is a single item).
+      const int nsplit = it.tail < 0 ? 1 : (it.n_union + a.pps - 1) / a.pps;
       if (it.n == 0) {
         // A tile with no usable block at all: out = 0, lse = -inf.
         if (it.split == 0 && it.n_union == 0 && active) {
@@ -667,7 +683,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         break;
       }
       tc_fence_after();
-      const size_t part = (unit * a.splits + it.split) * a.rows_part;
+      const size_t part = ((size_t)(it.tail < 0 ? 0 : it.tail) * a.splits + it.split) * a.rows_part;
       const bool has = l > 0.f;
       const float inv = has ? 1.f / l : 0.f;
 #pragma unroll
@@ -708,7 +724,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         a.part_ml[(part + row) * 2] = m_ref;
         a.part_ml[(part + row) * 2 + 1] = l;
       }
-      // The tile's splits are combined by merge_splits_kernel after this launch.
+      // The unit's splits are combined by merge_splits_kernel after this launch.
     }
   }
 
@@ -721,21 +737,43 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
 }
 
 
-// Combines the fp32 partials of tiles whose union was split across several
-// work items: for each (tile, KV head) unit and active row, with
+// Launches `kernel` so that it may start while the previous kernel on the
+// stream is finishing (programmatic dependent launch); the kernel itself
+// waits with grid_dependency_wait() before reading that kernel's results.
+template <class Kernel>
+cudaError_t launch_dependent(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             const PrefillArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+// Combines the fp32 partials of the tail units whose union was split across
+// several work items: for each such unit and active row, with
 // M = max_s m_s, L = sum_s 2^(m_s - M) l_s, out = sum_s 2^(m_s - M) O_s / L and
 // lse = (M + log2 L) ln 2 (m in log2 units of the scaled logits). One warp per
-// (unit, row); each lane owns four of the 128 dims.
+// (tail unit, row); each lane owns four of the 128 dims.
 __global__ void __launch_bounds__(256) merge_splits_kernel(const __grid_constant__ PrefillArgs a) {
+  grid_dependency_wait();  // partials of the attention kernel launched just before
   const int warp_global = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
-  const int units = a.num_kv_heads * a.max_tiles;
-  if (warp_global >= units * a.rows_part) return;
-  const int unit = warp_global / a.rows_part, row = warp_global - unit * a.rows_part;
-  const int h = unit / a.max_tiles, tile = unit - h * a.max_tiles;
+  if (warp_global >= a.tail_units * a.rows_part) return;
+  const int t = warp_global / a.rows_part, row = warp_global - t * a.rows_part;
+  const int unit = a.whole_units + t;
+  const int tile_idx = unit / a.num_kv_heads;
+  const int h = unit - tile_idx * a.num_kv_heads;
+  const int tile = a.max_tiles - 1 - tile_idx;
   const int t0 = __ldg(a.tile_info + 2 * tile);
   if (t0 < 0) return;
-  const int n_union = __ldg(a.union_len + unit);
+  const int n_union = __ldg(a.union_len + (size_t)h * a.max_tiles + tile);
   const int nsplit = (n_union + a.pps - 1) / a.pps;
   if (nsplit <= 1) return;  // written directly by the attention kernel
   const int G = a.num_qo_heads / a.num_kv_heads;
@@ -743,7 +781,7 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const __grid_constant
   const int nw = min(a.tile_tokens, __ldg(a.cu_q + b + 1) - t0);
   const int w = row / G, gh = row - w * G;
   if (row >= a.tile_tokens * G || w >= nw) return;
-  const size_t p0 = (size_t)unit * a.splits * a.rows_part + row;
+  const size_t p0 = (size_t)t * a.splits * a.rows_part + row;
   float M = -INFINITY;
   for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldg(a.part_ml + (p0 + (size_t)sp * a.rows_part) * 2));
   float L = 0.f;
@@ -778,12 +816,12 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   const int grid = a.num_items < device_sm_count() ? a.num_items : device_sm_count();
   if (grid <= 0) return cudaSuccess;
-  prefill_kernel<FP8, STREAM><<<grid, Roles<FP8>::kThreads, smem, s>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || a.splits <= 1) return e;
-  const long long warps = (long long)a.num_kv_heads * a.max_tiles * a.rows_part;
-  merge_splits_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  e = launch_dependent(prefill_kernel<FP8, STREAM>, dim3(grid), dim3(Roles<FP8>::kThreads), smem,
+                       s, a);
+  if (e != cudaSuccess || a.splits <= 1 || a.tail_units == 0) return e;
+  const long long warps = (long long)a.tail_units * a.rows_part;
+  return launch_dependent(merge_splits_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s,
+                          a);
 }
 
 }  // namespace
@@ -806,7 +844,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
   // Split launches are the memory-bound, decode-sized ones; their Q slots
   // share a region when a tile has at most 64 rows (whole 8-row groups).
   const int rows = a.tile_tokens * (a.num_qo_heads / a.num_kv_heads);
-  const bool stream = a.splits > 1 && rows <= 64 && rows % 8 == 0;
+  const bool stream = a.splits > 1 && a.tail_units > 0 && rows <= 64 && rows % 8 == 0;
   return stream ? launch_t<false, true>(a, s) : launch_t<false, false>(a, s);
 }
 

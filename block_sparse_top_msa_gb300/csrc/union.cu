@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(kUnionThreads)
   uint32_t* mem = reinterpret_cast<uint32_t*>(ulist + a.cap);  // W * words
   __shared__ int s_ulen;
 
+  grid_dependents_launch();
   int b = 0, t0 = 0;
   const bool live = locate_tile(a.cu_q, a.batch, a.tile_tokens, tile, scratch, &b, &t0);
   const size_t base = (size_t)h * a.max_tiles + tile;
@@ -148,6 +149,7 @@ __global__ void __launch_bounds__(1024) build_union_small_kernel(UnionArgs a) {
   __shared__ int s_warp[32];
   __shared__ int s_ulen;
 
+  grid_dependents_launch();
   int b = 0, t0 = 0;
   const bool live = locate_tile(a.cu_q, a.batch, a.tile_tokens, tile, scratch, &b, &t0);
   const size_t base = (size_t)h * a.max_tiles + tile;

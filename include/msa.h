@@ -182,10 +182,21 @@ int msa_union_tile_tokens(int num_qo_heads, int num_kv_heads);
 /*
  * Waits for `stream`, then returns and clears the library's device fault word
  * of the current device in *fault (0 = none). Kernels never trap: a wait that
- * exceeds its time limit, or an internal capacity check, sets a bit here and
- * the kernel returns early. Synchronises the host: for tests and diagnostics.
+ * exceeds its time limit (2 s), or an internal capacity check, sets a bit here
+ * and the kernel unwinds and returns. Bits: 1 a TMA copy never landed, 2 an
+ * MMA completion never came, 4 the softmax warps never released a buffer,
+ * 8 a capacity check failed, 16 another wait expired. Synchronises the host:
+ * for tests and diagnostics.
  */
 msa_status_t msa_read_device_fault(unsigned int* fault, cudaStream_t stream);
+
+/*
+ * Diagnostics: launches one CTA that waits, with a limit of timeout_us
+ * microseconds (1 .. 1000000), on a barrier nothing arrives at. The wait
+ * expires, fault bit 16 is set, and the kernel returns: the same path every
+ * bounded wait of the library takes instead of hanging.
+ */
+msa_status_t msa_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t stream);
 
 /*
  * Paged decode for callers that cannot allocate device memory (no counterpart
