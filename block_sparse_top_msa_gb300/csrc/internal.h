@@ -106,7 +106,7 @@ struct PrefillArgs {
   void* out;
   float* lse;
   // Work items, walked by a persistent grid. Units are (query tile, KV head)
-  // pairs, heaviest first. The first whole_units units are one item each and
+  // pairs, head-major with the heaviest tiles first within a head. The first whole_units units are one item each and
   // write out/lse directly. Each remaining ("tail") unit is split into
   // `splits` items, item s taking union entries [s*pps, (s+1)*pps); a tail
   // unit whose union needs more than one split writes fp32 partials

@@ -200,9 +200,11 @@ MSA_DEV Item item_at(const PrefillArgs& a, int i) {
     it.split = j - it.tail * a.splits;
     unit = a.whole_units + it.tail;
   }
-  const int tile_idx = unit / a.num_kv_heads;
-  it.h = unit - tile_idx * a.num_kv_heads;
-  it.tile = a.max_tiles - 1 - tile_idx;  // later (heavier) tiles first
+  // Head-major: all tiles of one KV head (later, heavier tiles first) before
+  // the next head, so the items in flight share one head's K/V in L2.
+  it.h = unit / a.max_tiles;
+  const int tile_idx = unit - it.h * a.max_tiles;
+  it.tile = a.max_tiles - 1 - tile_idx;
   it.t0 = __ldg(a.tile_info + 2 * it.tile);
   it.b = __ldg(a.tile_info + 2 * it.tile + 1);
   it.p_begin = it.tail < 0 ? 0 : it.split * a.pps;
@@ -768,9 +770,8 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const __grid_constant
   if (warp_global >= a.tail_units * a.rows_part) return;
   const int t = warp_global / a.rows_part, row = warp_global - t * a.rows_part;
   const int unit = a.whole_units + t;
-  const int tile_idx = unit / a.num_kv_heads;
-  const int h = unit - tile_idx * a.num_kv_heads;
-  const int tile = a.max_tiles - 1 - tile_idx;
+  const int h = unit / a.max_tiles;  // same head-major order as item_at
+  const int tile = a.max_tiles - 1 - (unit - h * a.max_tiles);
   const int t0 = __ldg(a.tile_info + 2 * tile);
   if (t0 < 0) return;
   const int n_union = __ldg(a.union_len + (size_t)h * a.max_tiles + tile);
