@@ -77,6 +77,30 @@ def barrier(world):
 
 
 # ---------------------------------------------------------------- measurement helpers
+# DRAM bytes per launch of the headline attention kernel, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum; see the profile named below).
+# Reported only while the kernel sources still hash to the fingerprint of the
+# build that was captured; otherwise the roofline's "traffic" is null.
+TRAFFIC_SOURCES = ("prefill.cu", "common.cuh", "tmem_wide.cuh", "internal.h", "tmap.h", "api.cu",
+                   "union.cu", "tile_map.cuh")
+TRAFFIC_MEASURED = {"fingerprint": "d1dbcccb215b3471", "bytes_per_launch": 2.433e9,
+                    "profile": "profiles/prefill_kernel_flat_varlen_2x32768_traffic.md"}
+
+
+def kernel_fingerprint():
+    import hashlib
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "block_sparse_top_msa_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic():
+    if kernel_fingerprint() == TRAFFIC_MEASURED["fingerprint"]:
+        return TRAFFIC_MEASURED["bytes_per_launch"]
+    return None
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -239,6 +263,9 @@ def bench_prefill(msa, args, device, world, rank):
     flops = 4.0 * D * G * float(cnt.sum())
     blocks = (inp["q2k_indices"] >= 0).sum().item()
     flops_block = 4.0 * D * G * 128 * float(blocks)
+    # Bytes the attention kernel must move at least once: q and K/V read, out written.
+    alg_bytes = (inp["q"].numel() * inp["q"].element_size() * 2 +
+                 (inp["k"].numel() + inp["v"].numel()) * inp["k"].element_size())
     out = torch.empty_like(inp["q"])
     lse = torch.empty((tq, hq), dtype=torch.float32, device=device)
     need = msa.msa_sparse_attention_workspace_size(len(inp["lengths"]), tq, hq, hkv, D, 16,
@@ -282,7 +309,10 @@ def bench_prefill(msa, args, device, world, rank):
         value=aggregate_value(flops, world, step_s) / 1e12, clocks=clk.summary(), fault=fault,
         roofline={"bound": "tensor", "achieved": round(achieved, 2),
                   "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                  "frac": round(achieved / pk["bf16_sus"], 4), "traffic": None,
+                  "frac": round(achieved / pk["bf16_sus"], 4),
+                  "traffic": None if args.profile_small else measured_traffic(),
+                  "traffic_source": TRAFFIC_MEASURED["profile"],
+                  "algorithmic_bytes": int(alg_bytes),
                   "kernel": "prefill_kernel<bf16>",
                   "peak_kind": f"bf16_tflops_sustained ({pk['source']})",
                   "achieved_is": "algorithmic FLOP per launch / mean launch time"},
