@@ -32,29 +32,54 @@
 namespace msa {
 namespace {
 
-constexpr int kKStagesMax = 3;  // K ring (a slot frees when its QK completes)
 constexpr int kF8Stages = 2;    // E4M3 staging ring (K and V bytes of one block)
 constexpr int kSBuf = 3;        // S/P buffers in TMEM: QK runs two blocks ahead of PV
+constexpr int kPV = 3;          // PV completion barriers (block g uses g % kPV)
 constexpr int kTile = 16384;    // bytes of one 128-row x 128-byte swizzled tile
 constexpr float kRescaleLog2 = 8.0f;
 
-// TMEM column map (512 columns allocated): S_b at 128*b for b = 0..2 (its P,
-// packed bf16 pairs, overwrites the first 64 columns of S_b once the softmax
-// has read S_b), O at 384.
+// TMEM column map (512 columns allocated): S_b at 128*b for b = 0..2, O at
+// 384. P (packed bf16 pairs) overwrites S_b once the softmax has read it: the
+// P of S columns 64j..64j+63 goes to columns 64j..64j+31, inside the column
+// group its softmax warpgroup owns.
 constexpr uint32_t kColO = 384;
 
-// STREAM: layout for memory-bound launches (decode-sized problems split into
-// many short items, at most 64 real Q rows). Their two Q slots share one
-// 32 KiB region, slot j starting j * rows * 128 bytes in: each slot's real
-// rows stay clear of the other's, and the rows an M=128 MMA reads past them
-// (other slots, or the K ring) only feed S rows no token owns. That leaves
-// room for a four-deep V ring. Otherwise two separate Q buffers.
+// Shared memory holds one Q tile, a three-deep K ring and a three-deep V ring
+// (bf16). STREAM: layout for memory-bound launches (decode-sized problems
+// split into many short items, at most 64 real Q rows): two Q slots share the
+// one 32 KiB Q region, slot j starting j * rows * 128 bytes in, so the next
+// item's Q loads while the current one runs; each slot's real rows stay clear
+// of the other's, and the rows an M=128 MMA reads past them (other slots, or
+// the K ring) only feed S rows no token owns.
+//
+// Completion barriers: qk_done[g % 3] completes when QK(g) (and every MMA
+// issued before it) has completed: S_g is readable and the K slot of block g
+// is free. pv_done[g % 3] likewise for PV(g): O holds block g and its V slot
+// is free. One commit per MMA group keeps the issuing thread's overhead low.
+// Warp roles. The softmax runs in kSoftmaxWG warpgroups; with two, warps q
+// and q + 4 share TMEM lanes 32q..32q+31 and split each S row by columns
+// (0..63 and 64..127), exchanging their partial row maxima every block. The
+// E4M3 variant keeps one warpgroup: its converter warps need the registers.
+template <bool FP8>
+struct Roles {
+  static constexpr int kSoftmaxWG = FP8 ? 1 : 2;
+  static constexpr int kSoftmaxWarps = 4 * kSoftmaxWG;
+  static constexpr int kProducerWarp = kSoftmaxWarps;              // Q and K (E4M3: K and V)
+  static constexpr int kMmaWarp = kSoftmaxWarps + 1;
+  static constexpr int kVProducerWarp = FP8 ? -1 : kSoftmaxWarps + 2;  // V (bf16 only)
+  static constexpr int kConvWarp0 = kSoftmaxWarps + 2;              // E4M3 converters
+  static constexpr int kWarps = kSoftmaxWarps + (FP8 ? 6 : 3);
+  static constexpr int kThreads = kWarps * 32;
+};
+
 template <bool FP8, bool STREAM = false>
 struct __align__(1024) PrefillSmem {
-  static constexpr int kQBuf = FP8 ? 1 : 2;                       // Q tiles of consecutive items
-  static constexpr int kQRegions = STREAM ? 1 : kQBuf;
-  static constexpr int kKStages = STREAM ? 3 : 2;                 // K ring (frees when its QK completes)
-  static constexpr int kVStages = FP8 ? 2 : 3;                    // V ring (frees when its PV completes)
+  static constexpr int kXch = Roles<FP8>::kSoftmaxWG == 2 ? 2 * 2 * 128 : 1;
+  static constexpr int kQBuf = STREAM ? 2 : 1;   // Q tiles of consecutive items
+  static constexpr int kQRegions = 1;
+  static constexpr int kKStages = FP8 ? 2 : 3;   // K ring (a slot frees when its QK completes)
+  static constexpr int kVStages = FP8 ? 2 : 3;   // V ring (a slot frees when its PV completes)
+  static_assert(kKStages <= kSBuf && kVStages <= kPV, "ring deeper than its completion barriers");
   uint8_t q[kQRegions][2][kTile];
   uint8_t k[kKStages][2][kTile];
   uint8_t v[kVStages][2][kTile];
@@ -62,35 +87,38 @@ struct __align__(1024) PrefillSmem {
   uint8_t v8[FP8 ? kF8Stages : 1][FP8 ? kTile : 16];
   uint64_t q_full[kQBuf];
   uint64_t q_empty[kQBuf];
-  uint64_t k_full[kKStagesMax];
-  uint64_t k_empty[kKStagesMax];
+  uint64_t k_full[kKStages];
   uint64_t v_full[kVStages];
-  uint64_t v_empty[kVStages];
   uint64_t f8_full[kF8Stages];
   uint64_t f8_empty[kF8Stages];
-  uint64_t s_full[kSBuf];
+  uint64_t qk_done[kSBuf];
   uint64_t p_full[kSBuf];
-  uint64_t o_done[2];
+  uint64_t pv_done[kPV];
   uint64_t o_free;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-};
-
-template <bool FP8>
-struct Roles {
-  static constexpr int kSoftmaxWarps = 4;
-  static constexpr int kProducerWarp = 4;
-  static constexpr int kMmaWarp = 5;
-  static constexpr int kConvWarp0 = 6;
-  static constexpr int kWarps = FP8 ? 10 : 6;
-  static constexpr int kThreads = kWarps * 32;
+  float xch[kXch];  // [slot][warpgroup][row] values exchanged between the softmax warpgroups
 };
 
 MSA_DEV float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Named barrier of softmax warps q and q + 4 (64 threads, barrier q + 1);
+// returns the AND of p over both warps. Both warps of a pair take the same
+// branches (their decisions are made from exchanged values), so each arrives.
+MSA_DEV bool pair_barrier_and(int q, bool p) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.s32 pi, %1, 0;\n\t"
+      "bar.red.and.pred po, %2, 64, pi;\n\tselp.s32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"((int)p), "r"(q + 1)
+      : "memory");
+  return r != 0;
 }
 
 MSA_DEV float fmax3(float a, float b, float c) {
@@ -113,7 +141,6 @@ MSA_DEV float row_max64(const float* v) {
   m1 = fmax3(m1, v[62], v[63]);
   return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
-MSA_DEV float row_max128(const float* v) { return fmaxf(row_max64(v), row_max64(v + 64)); }
 
 // Running-max update of one row for a block whose raw max logit is mx. The
 // reference max only moves when the new max exceeds it by more than 2^8, so
@@ -187,7 +214,16 @@ struct Item {
   int seq_q0, lq, lk, kv0;  // the tile's sequence (valid when t0 >= 0)
 };
 
-MSA_DEV Item item_at(const PrefillArgs& a, int i) {
+// The (t0, b) pair of item i's tile, the one field that needs a load before
+// the rest can be fetched (and that the softmax warps fetch one item ahead).
+MSA_DEV int2 item_tile_info(const PrefillArgs& a, int i) {
+  const int unit = i < a.whole_units ? i : a.whole_units + (i - a.whole_units) / a.splits;
+  const int h = unit / a.max_tiles;
+  const int tile = a.max_tiles - 1 - (unit - h * a.max_tiles);
+  return __ldg(reinterpret_cast<const int2*>(a.tile_info) + tile);
+}
+
+MSA_DEV Item item_at(const PrefillArgs& a, int i, int2 ti) {
   Item it;
   int unit;
   if (i < a.whole_units) {
@@ -205,8 +241,8 @@ MSA_DEV Item item_at(const PrefillArgs& a, int i) {
   it.h = unit / a.max_tiles;
   const int tile_idx = unit - it.h * a.max_tiles;
   it.tile = a.max_tiles - 1 - tile_idx;
-  it.t0 = __ldg(a.tile_info + 2 * it.tile);
-  it.b = __ldg(a.tile_info + 2 * it.tile + 1);
+  it.t0 = ti.x;
+  it.b = ti.y;
   it.p_begin = it.tail < 0 ? 0 : it.split * a.pps;
   it.n_union = 0;
   it.n = 0;
@@ -244,7 +280,7 @@ MSA_DEV void cursor_next(const PrefillArgs& a, Cursor& c) {
       c.valid = false;
       return;
     }
-    c.it = item_at(a, c.i);
+    c.it = item_at(a, c.i, item_tile_info(a, c.i));
     c.u = 0;
     if (c.it.n > 0) ++c.k;
   }
@@ -269,10 +305,35 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   constexpr int kKStages = Smem::kKStages;
   constexpr int kVStages = Smem::kVStages;
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                      ~uintptr_t(1023));
+  // The swizzled tiles need a 1024-byte aligned base; the launch reserves up
+  // to 1 KiB of slack for it when the limit leaves room. A launch whose slack
+  // does not cover the base's actual offset reports and does nothing.
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  {
+    uint32_t dyn;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+    if (pad + sizeof(Smem) > dyn) {
+      if (threadIdx.x == 0) atomicOr(a.fault, (unsigned)kFaultCapacity);
+      return;
+    }
+  }
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw + pad);
   unsigned* fault = a.fault;
   volatile int* abort = &sm.abort;
+  // Waits until QK(j) / PV(j), the j-th block's MMA group of this CTA, has
+  // completed. Block j - 3 used the same barrier one phase earlier, and every
+  // caller has already seen it complete (MMAs complete in issue order, and
+  // each caller waits for blocks in increasing order; the softmax and the
+  // epilogue wait for QK(gg) first, which is issued after PV(gg - 3)), so the
+  // parity names the right phase. No barrier can run a phase ahead of a
+  // waiter either: QK(j + 3) and PV(j + 3) need data the waiter has not
+  // released yet.
+  auto qk_wait = [&](int j) {
+    return mbar_wait(&sm.qk_done[j % kSBuf], (j / kSBuf) & 1, fault, kFaultWaitMma, abort);
+  };
+  auto pv_wait = [&](int j) {
+    return mbar_wait(&sm.pv_done[j % kPV], (j / kPV) & 1, fault, kFaultWaitMma, abort);
+  };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.num_qo_heads / a.num_kv_heads;
   const int W = a.tile_tokens;
@@ -289,22 +350,20 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     }
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&sm.k_full[s], FP8 ? 4 : 1);
-      mbar_init(&sm.k_empty[s], 1);
     }
     for (int s = 0; s < kVStages; ++s) {
       mbar_init(&sm.v_full[s], FP8 ? 4 : 1);
-      mbar_init(&sm.v_empty[s], 1);
     }
     for (int s = 0; s < kF8Stages; ++s) {
       mbar_init(&sm.f8_full[s], 1);
       mbar_init(&sm.f8_empty[s], 4);
     }
     for (int s = 0; s < kSBuf; ++s) {
-      mbar_init(&sm.s_full[s], 1);
-      mbar_init(&sm.p_full[s], 4);
+      mbar_init(&sm.qk_done[s], 1);
+      mbar_init(&sm.p_full[s], R::kSoftmaxWarps);
     }
-    for (int s = 0; s < 2; ++s) mbar_init(&sm.o_done[s], 1);
-    mbar_init(&sm.o_free, 4);
+    for (int s = 0; s < kPV; ++s) mbar_init(&sm.pv_done[s], 1);
+    mbar_init(&sm.o_free, R::kSoftmaxWarps);
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
     fence_mbar_init();
@@ -322,9 +381,13 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   grid_dependency_wait();
   grid_dependents_launch();
 
-  if (warp == R::kProducerWarp) {
-    // ------------------------------------------------------------ producer
+  if (warp == R::kProducerWarp || warp == R::kVProducerWarp) {
+    // ------------------------------------------------------------ producers
+    // One thread issues the Q tiles and the K blocks (for E4M3: both K and V
+    // bytes into the staging ring); for bf16 a second warp issues the V
+    // blocks, so that a K load never queues behind a V slot still in use.
     if (lane == 0) {
+      const bool kq = warp == R::kProducerWarp;
       tma_prefetch_desc(&a.tmap_q);
       tma_prefetch_desc(&a.tmap_k);
       tma_prefetch_desc(&a.tmap_v);
@@ -336,17 +399,19 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       bool ok = true;
       int g = 0, k = 0;  // blocks issued, non-empty items seen
       for (int i = blockIdx.x; ok && i < a.num_items; i += gridDim.x) {
-        const Item it = item_at(a, i);
+        const Item it = item_at(a, i, item_tile_info(a, i));
         if (it.n == 0) continue;
-        const int qb = k % kQBuf;
-        if (k >= kQBuf &&
-            !mbar_wait(&sm.q_empty[qb], ((k / kQBuf) - 1) & 1, fault, kFaultWaitMma, abort)) {
-          ok = false;
-          break;
+        if (kq) {
+          const int qb = k % kQBuf;
+          if (k >= kQBuf &&
+              !mbar_wait(&sm.q_empty[qb], ((k / kQBuf) - 1) & 1, fault, kFaultWaitMma, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&sm.q_full[qb], 2u * 128u * (uint32_t)(G * W));
+          for (int c = 0; c < 2; ++c)
+            tma_load_3d(q_addr(qb, c), &a.tmap_q, &sm.q_full[qb], c * 64, it.h * G, it.t0);
         }
-        mbar_expect_tx(&sm.q_full[qb], 2u * 128u * (uint32_t)(G * W));
-        for (int c = 0; c < 2; ++c)
-          tma_load_3d(q_addr(qb, c), &a.tmap_q, &sm.q_full[qb], c * 64, it.h * G, it.t0);
         const int32_t* ulist =
             a.union_blocks + ((size_t)it.h * a.max_tiles + it.tile) * a.cap + it.p_begin;
         for (int u = 0; u < it.n; ++u, ++g) {
@@ -358,31 +423,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
             if (page < 0 || page >= a.num_pages) page = a.num_pages;
           }
           const int row = it.kv0 + blk * kBlk;
-          if (!FP8) {
-            const int ks = g % kKStages, vs = g % kVStages;
-            if (g >= kKStages && !mbar_wait(&sm.k_empty[ks], ((g / kKStages) - 1) & 1, fault,
-                                            kFaultWaitMma, abort)) {
-              ok = false;
-              break;
-            }
-            mbar_expect_tx(&sm.k_full[ks], 2 * kTile);
-            for (int c = 0; c < 2; ++c) {
-              if (a.paged) tma_load_4d(sm.k[ks][c], &a.tmap_k, &sm.k_full[ks], c * 64, 0, it.h, page);
-              else tma_load_3d(sm.k[ks][c], &a.tmap_k, &sm.k_full[ks], c * 64, it.h, row);
-            }
-            last_k[ks] = g;
-            if (g >= kVStages && !mbar_wait(&sm.v_empty[vs], ((g / kVStages) - 1) & 1, fault,
-                                            kFaultWaitMma, abort)) {
-              ok = false;
-              break;
-            }
-            mbar_expect_tx(&sm.v_full[vs], 2 * kTile);
-            for (int c = 0; c < 2; ++c) {
-              if (a.paged) tma_load_4d(sm.v[vs][c], &a.tmap_v, &sm.v_full[vs], c * 64, 0, it.h, page);
-              else tma_load_3d(sm.v[vs][c], &a.tmap_v, &sm.v_full[vs], c * 64, it.h, row);
-            }
-            last_v[vs] = g;
-          } else {
+          if (FP8) {
             const int s8 = g % kF8Stages;
             if (g >= kF8Stages && !mbar_wait(&sm.f8_empty[s8], ((g / kF8Stages) - 1) & 1, fault,
                                              kFaultWaitOther, abort)) {
@@ -398,6 +439,30 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
               tma_load_3d(sm.v8[s8], &a.tmap_v, &sm.f8_full[s8], 0, it.h, row);
             }
             last_8[s8] = g;
+          } else if (kq) {
+            const int ks = g % kKStages;
+            if (g >= kKStages && !qk_wait(g - kKStages)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&sm.k_full[ks], 2 * kTile);
+            for (int c = 0; c < 2; ++c) {
+              if (a.paged) tma_load_4d(sm.k[ks][c], &a.tmap_k, &sm.k_full[ks], c * 64, 0, it.h, page);
+              else tma_load_3d(sm.k[ks][c], &a.tmap_k, &sm.k_full[ks], c * 64, it.h, row);
+            }
+            last_k[ks] = g;
+          } else {
+            const int vs = g % kVStages;
+            if (g >= kVStages && !pv_wait(g - kVStages)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&sm.v_full[vs], 2 * kTile);
+            for (int c = 0; c < 2; ++c) {
+              if (a.paged) tma_load_4d(sm.v[vs][c], &a.tmap_v, &sm.v_full[vs], c * 64, 0, it.h, page);
+              else tma_load_3d(sm.v[vs][c], &a.tmap_v, &sm.v_full[vs], c * 64, it.h, row);
+            }
+            last_v[vs] = g;
           }
         }
         ++k;
@@ -433,8 +498,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
           const uint64_t bd = sdesc_sw128(smem_u32(sm.k[ks][kk >> 2]) + (kk & 3) * 32, 16, 1024);
           mma_ss(tbase + b * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&sm.s_full[b]);
-        mma_commit(&sm.k_empty[ks]);
+        mma_commit(&sm.qk_done[c.g % kSBuf]);
         if (c.u == c.it.n - 1) mma_commit(&sm.q_empty[qb]);
         return true;
       };
@@ -452,10 +516,10 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t bd = sdesc_sw128(smem_u32(sm.v[vs][0]) + kk * 2048, kTile, 1024);
-          mma_ts(tbase + kColO, tbase + b * 128 + kk * 8, bd, idO, (c.u > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t pcol = b * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
+          mma_ts(tbase + kColO, tbase + pcol, bd, idO, (c.u > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&sm.o_done[c.g & 1]);
-        mma_commit(&sm.v_empty[vs]);
+        mma_commit(&sm.pv_done[c.g % kPV]);
         return true;
       };
       Cursor qc, pc;
@@ -484,12 +548,11 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     int g = 0;
     bool ok = true;
     for (int i = blockIdx.x; ok && i < a.num_items; i += gridDim.x) {
-      const Item it = item_at(a, i);
+      const Item it = item_at(a, i, item_tile_info(a, i));
       for (int u = 0; u < it.n; ++u, ++g) {
         const int s8 = g % kF8Stages, ks = g % kKStages, vs = g % kVStages;
         if (!mbar_wait(&sm.f8_full[s8], (g / kF8Stages) & 1, fault, kFaultWaitTma, abort) ||
-            (g >= kKStages && !mbar_wait(&sm.k_empty[ks], ((g / kKStages) - 1) & 1, fault,
-                                         kFaultWaitMma, abort))) {
+            (g >= kKStages && !qk_wait(g - kKStages))) {
           ok = false;
           break;
         }
@@ -497,8 +560,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.k_full[ks]);
-        if (g >= kVStages && !mbar_wait(&sm.v_empty[vs], ((g / kVStages) - 1) & 1, fault,
-                                        kFaultWaitMma, abort)) {
+        if (g >= kVStages && !pv_wait(g - kVStages)) {
           ok = false;
           break;
         }
@@ -513,18 +575,34 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     }
   } else if (warp < R::kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int row = tid;  // TMEM lane
+    constexpr int NW = R::kSoftmaxWG;
+    constexpr int kHalves = 2 / NW;   // 64-column halves of S and O per warp
+    const int q4 = warp & 3;          // TMEM lane quarter
+    const int wg = warp >> 2;         // column group (with NW == 2: columns 64*wg..64*wg+63)
+    const int row = q4 * 32 + lane;   // TMEM lane
     const int w = row / G, gh = row - w * G;
-    const uint32_t lane_base = tbase + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane_base = tbase + ((uint32_t)(q4 * 32) << 16);
     const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
     bool ok = true;
-    int g = 0;  // blocks consumed
+    int g = 0;   // blocks consumed
+    int xi = 0;  // exchanges with the partner warp so far (two alternating slots)
+    // Publishes v to the partner warp (same lanes, other column group) and
+    // returns the partner's value; okv becomes the AND over both warps. A
+    // slot is rewritten two exchanges later, after the partner has passed the
+    // barrier that follows its read.
+    auto exchange = [&](float v, bool& okv) -> float {
+      float* slot = sm.xch + (xi & 1) * 256;
+      slot[wg * 128 + row] = v;
+      okv = pair_barrier_and(q4, okv);
+      ++xi;
+      return slot[(1 - wg) * 128 + row];
+    };
     int i = blockIdx.x;
-    Item nxt = i < a.num_items ? item_at(a, i) : Item{};
+    int2 nti = i < a.num_items ? item_tile_info(a, i) : make_int2(-1, 0);
     for (; ok && i < a.num_items; i += gridDim.x) {
-      const Item it = nxt;
-      // The next item's metadata is fetched while this one runs.
-      if (i + (int)gridDim.x < a.num_items) nxt = item_at(a, i + gridDim.x);
+      const Item it = item_at(a, i, nti);
+      // The next item's tile is fetched while this one runs.
+      if (i + (int)gridDim.x < a.num_items) nti = item_tile_info(a, i + gridDim.x);
       if (it.t0 < 0) continue;
       const int nw = min(W, it.seq_q0 + it.lq - it.t0);
       const bool active = row < W * G && w < nw;
@@ -536,8 +614,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         if (it.split == 0 && it.n_union == 0 && active) {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * 128);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) dst[c] = make_uint4(0u, 0u, 0u, 0u);
-          if (a.lse != nullptr) a.lse[orow] = -INFINITY;
+          for (int c = 0; c < 8 * kHalves; ++c) dst[wg * 8 * kHalves + c] = make_uint4(0u, 0u, 0u, 0u);
+          if (wg == 0 && a.lse != nullptr) a.lse[orow] = -INFINITY;
         }
         continue;
       }
@@ -545,7 +623,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       const size_t unit = (size_t)it.h * a.max_tiles + it.tile;
       const uint32_t* mrow = a.member + (unit * W + (active ? w : 0)) * a.words;
       const int32_t* ulist = a.union_blocks + unit * a.cap + it.p_begin;
-      float m_ref = -INFINITY, l = 0.f;
+      float m_ref = -INFINITY, l = 0.f;  // l: sum over this warp's columns
       // Per-block metadata for block u, fetched one block ahead.
       uint32_t mword = active ? __ldg(mrow + (it.p_begin >> 5)) : 0u;
       int nblk_id = __ldg(ulist);
@@ -577,34 +655,45 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         }
         // QK(gg) done: S is readable, and every PV up to gg-3 (the last user
         // of this P buffer) has completed.
-        ok = mbar_wait(&sm.s_full[bb], (gg / kSBuf) & 1, fault, kFaultWaitMma, abort);
-        if (__any_sync(0xffffffffu, !ok)) {
-          ok = false;
-          break;
-        }
+        ok = qk_wait(gg);
+        ok = !__any_sync(0xffffffffu, !ok);
+        if (NW == 1 && !ok) break;
         tc_fence_after();
         const bool warp_mem = __any_sync(0xffffffffu, mem);
         const bool warp_masked = __any_sync(0xffffffffu, mem && lim < 127);
-        const uint32_t scol = lane_base + bb * 128;  // S_b, and P_b in its first 64 columns
+        const uint32_t scol = lane_base + bb * 128;  // S_b; P_b in columns 0..31 and 64..95
         float alpha = 1.f;
         bool rescale = false;
-        if (warp_mem) {
-          float2 acc = make_float2(0.f, 0.f);
-          if (!FP8) {
-            float sv[128];
-            tmem_ld128(scol, sv);
+        float2 acc = make_float2(0.f, 0.f);
+        if constexpr (NW == 2) {
+          const uint32_t gcol = scol + wg * 64;  // this warp's 64 S columns; its P: the first 32
+          float sv[64];
+          float mx = -INFINITY;
+          if (ok && warp_mem) {
+            tmem_ld64(gcol, sv);
             if (warp_masked) {
 #pragma unroll
-              for (int c = 0; c < 128; ++c)
-                if (c > lim) sv[c] = -INFINITY;
+              for (int c = 0; c < 64; ++c)
+                if (wg * 64 + c > lim) sv[c] = -INFINITY;
             }
-            const float mx = row_max128(sv);
+            mx = row_max64(sv);
+          }
+          mx = fmaxf(mx, exchange(mx, ok));
+          if (!ok) break;
+          if (warp_mem) {
             update_max(mem, mx, a.scale_log2, m_ref, l, alpha, rescale);
             // Non-member rows use -inf as their offset, so every P entry is 0.
             const float neg_m = mem ? -m_ref : -INFINITY;
-            exp_pack_store<64>(sv, sc2, neg_m, acc, scol);
-            exp_pack_store<64>(sv + 64, sc2, neg_m, acc, scol + 32);
+            exp_pack_store<64>(sv, sc2, neg_m, acc, gcol);
           } else {
+            // QK(gg) overwrote this buffer: P must be rewritten (zeros) every block.
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) pk[c] = 0u;
+            tmem_st32(gcol, pk);
+          }
+        } else {
+          if (warp_mem) {
             float mx = -INFINITY;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -619,52 +708,44 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
             }
             update_max(mem, mx, a.scale_log2, m_ref, l, alpha, rescale);
             const float neg_m = mem ? -m_ref : -INFINITY;
-            // Columns 64..127 of S are read before P's second half (columns
-            // 32..63) is written over them.
-            float sh[64];
-            tmem_ld64(scol + 64, sh);
-            {
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
               float sv[64];
-              tmem_ld64(scol, sv);
+              tmem_ld64(scol + half * 64, sv);
               if (warp_masked) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
-                  if (c > lim) sv[c] = -INFINITY;
+                  if (half * 64 + c > lim) sv[c] = -INFINITY;
               }
-              exp_pack_store<64>(sv, sc2, neg_m, acc, scol);
+              // Written over columns of this half that were just read.
+              exp_pack_store<64>(sv, sc2, neg_m, acc, scol + half * 64);
             }
-            if (warp_masked) {
+          } else {
+            uint32_t pk[32];
 #pragma unroll
-              for (int c = 0; c < 64; ++c)
-                if (64 + c > lim) sh[c] = -INFINITY;
-            }
-            exp_pack_store<64>(sh, sc2, neg_m, acc, scol + 32);
+            for (int c = 0; c < 32; ++c) pk[c] = 0u;
+            tmem_st32(scol, pk);
+            tmem_st32(scol + 64, pk);
           }
-          if (mem) l += acc.x + acc.y;
-        } else {
-          // QK(gg) overwrote this buffer: P must be rewritten (zeros) every block.
-          uint32_t pk[64];
-#pragma unroll
-          for (int c = 0; c < 64; ++c) pk[c] = 0u;
-          tmem_st64(scol, pk);
         }
+        if (mem) l += acc.x + acc.y;
+        // Rows rescale identically in both warps of a pair (same maxima).
         if (__any_sync(0xffffffffu, rescale)) {
           // O must hold every PV of this item up to gg-1 before it is rescaled.
-          ok = mbar_wait(&sm.o_done[(gg - 1) & 1], ((gg - 1) >> 1) & 1, fault, kFaultWaitMma,
-                         abort);
-          if (__any_sync(0xffffffffu, !ok)) {
-            ok = false;
-            break;
-          }
+          ok = pv_wait(gg - 1);
+          ok = !__any_sync(0xffffffffu, !ok);
+          if (NW == 2) ok = pair_barrier_and(q4, ok);
+          if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
+          for (int hh = 0; hh < kHalves; ++hh) {
+            const uint32_t ocol = lane_base + kColO + (wg * kHalves + hh) * 64;
             float o[64];
-            tmem_ld64(lane_base + kColO + half * 64, o);
+            tmem_ld64(ocol, o);
             uint32_t ow[64];
 #pragma unroll
             for (int c = 0; c < 64; ++c) ow[c] = __float_as_uint(o[c] * alpha);
-            tmem_st64(lane_base + kColO + half * 64, ow);
+            tmem_st64(ocol, ow);
           }
         }
         tc_fence_before();
@@ -673,23 +754,19 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       }
       if (!ok) break;
       // ---------------------------------------------------- item epilogue
-      // PV(glast - 1) first: its completion implies PV(glast - 2)'s, which
-      // makes the wait on PV(glast)'s barrier phase unambiguous.
       const int glast = g + it.n - 1;
-      if (glast >= 1)
-        ok = mbar_wait(&sm.o_done[(glast - 1) & 1], ((glast - 1) >> 1) & 1, fault, kFaultWaitMma,
-                       abort);
-      if (ok) ok = mbar_wait(&sm.o_done[glast & 1], (glast >> 1) & 1, fault, kFaultWaitMma, abort);
-      if (__any_sync(0xffffffffu, !ok)) {
-        ok = false;
-        break;
-      }
+      ok = pv_wait(glast);
+      ok = !__any_sync(0xffffffffu, !ok);
+      float lt = l;  // the row's full sum
+      if constexpr (NW == 2) lt += exchange(l, ok);
+      if (!ok) break;
       tc_fence_after();
       const size_t part = ((size_t)(it.tail < 0 ? 0 : it.tail) * a.splits + it.split) * a.rows_part;
-      const bool has = l > 0.f;
-      const float inv = has ? 1.f / l : 0.f;
+      const bool has = lt > 0.f;
+      const float inv = has ? 1.f / lt : 0.f;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int hh = 0; hh < kHalves; ++hh) {
+        const int half = wg * kHalves + hh;
         float o[64];
         tmem_ld64(lane_base + kColO + half * 64, o);
         if (!active) continue;
@@ -717,16 +794,14 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.o_free);
       g += it.n;
+      if (!active || wg != 0) continue;
       if (nsplit == 1) {
-        if (active && a.lse != nullptr)
-          a.lse[orow] = has ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        if (a.lse != nullptr) a.lse[orow] = has ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
         continue;
       }
-      if (active) {
-        a.part_ml[(part + row) * 2] = m_ref;
-        a.part_ml[(part + row) * 2 + 1] = l;
-      }
       // The unit's splits are combined by merge_splits_kernel after this launch.
+      a.part_ml[(part + row) * 2] = m_ref;
+      a.part_ml[(part + row) * 2 + 1] = lt;
     }
   }
 
@@ -811,8 +886,16 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const __grid_constant
 
 template <bool FP8, bool STREAM>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
-  const size_t smem = sizeof(PrefillSmem<FP8, STREAM>) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<FP8, STREAM>,
+  // Up to 1 KiB of slack for aligning the base, within the per-block limit
+  // (the kernel checks that the slack it got covers its base's offset).
+  int optin = 0, dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  size_t smem = sizeof(PrefillSmem<FP8, STREAM>) + 1024;
+  if (smem > (size_t)optin) smem = (size_t)optin;
+  e = cudaFuncSetAttribute(prefill_kernel<FP8, STREAM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = a.num_items < device_sm_count() ? a.num_items : device_sm_count();
