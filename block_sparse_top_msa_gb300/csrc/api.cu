@@ -79,16 +79,22 @@ PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk, 
   L.tail_units = 0;
   L.splits = 1;
   L.pps = L.cap;
+  // The split count minimises the tail's length in blocks: rounds of pieces
+  // over the SMs times the piece size, plus one block per item for its start
+  // and hand-over (pieces are dealt round-robin, one per SM and round).
   const long long rem = units % kPlanSMs;
   if (rem > 0) {
-    int S = (int)((kPlanSMs + rem - 1) / rem);
-    if (S > bound) S = bound;
-    if (S > 1) {
+    long long best_cost = ((rem + kPlanSMs - 1) / kPlanSMs) * (long long)(bound + 1);
+    for (int S = 2; S <= bound; ++S) {
       int pps = (bound + S - 1) / S;
       if (pps < kMinSplitBlocks) pps = kMinSplitBlocks;
-      S = (bound + pps - 1) / pps;
-      if (S > 1) {
-        L.splits = S;
+      const int s_eff = (bound + pps - 1) / pps;
+      if (s_eff < 2) continue;
+      const long long rounds = (rem * s_eff + kPlanSMs - 1) / kPlanSMs;
+      const long long cost = rounds * (pps + 1);
+      if (cost < best_cost) {
+        best_cost = cost;
+        L.splits = s_eff;
         L.pps = pps;
         L.tail_units = (int)rem;
         L.whole_units = (int)(units - rem);

@@ -35,6 +35,7 @@ namespace {
 constexpr int kF8Stages = 2;    // E4M3 staging ring (K and V bytes of one block)
 constexpr int kSBuf = 3;        // S/P buffers in TMEM: QK runs two blocks ahead of PV
 constexpr int kPV = 3;          // PV completion barriers (block g uses g % kPV)
+static_assert(kPV == kSBuf, "the MMA issuer walks S buffers and PV barriers with one ring");
 constexpr int kTile = 16384;    // bytes of one 128-row x 128-byte swizzled tile
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -265,6 +266,20 @@ MSA_DEV Item item_at(const PrefillArgs& a, int i, int2 ti) {
 // Position in the CTA's stream of blocks: item index i (stride gridDim.x),
 // block u inside the item, ordinal k of the item among non-empty items, and
 // global block ordinal g.
+// Slot index and phase parity of a position in a ring of N slots, advanced
+// one step at a time (no divisions on the MMA issue path).
+template <int N>
+struct RingPos {
+  int idx = 0;
+  uint32_t phase = 0;
+  MSA_DEV void next() {
+    if (++idx == N) {
+      idx = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 struct Cursor {
   int i, u, k, g;
   bool valid;
@@ -485,41 +500,60 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       const uint32_t idO = idesc_bf16_f32(128, 128, false, true);
       bool ok = true;
+      // Descriptors of slot 0; a slot or K step only moves the start-address
+      // field (16-byte units), so the issue path adds constants.
+      constexpr uint32_t kSlot16 = (2 * kTile) >> 4;  // one K or V slot
+      constexpr uint32_t kHalf16 = kTile >> 4;        // second 64-column half
+      const uint64_t dq0 = sdesc_sw128(smem_u32(q_addr(0, 0)), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(smem_u32(&sm.k[0][0][0]), 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(smem_u32(&sm.v[0][0][0]), kTile, 1024);
+      const uint32_t qslot16 = STREAM ? ((uint32_t)(W * G) * 128u) >> 4 : 0u;
+      // Ring positions of the QK stream and of the PV stream.
+      RingPos<kQBuf> rq;
+      RingPos<kKStages> rk;
+      RingPos<kSBuf> rs;
+      RingPos<kVStages> rv;
+      RingPos<kSBuf> rp;
+      uint32_t ofree_phase = 0;
       auto issue_qk = [&](const Cursor& c) -> bool {
-        const int qb = c.k % kQBuf, ks = c.g % kKStages, b = c.g % kSBuf;
-        if (c.u == 0 && !mbar_wait(&sm.q_full[qb], (c.k / kQBuf) & 1, fault, kFaultWaitTma, abort))
+        if (c.u == 0 && !mbar_wait(&sm.q_full[rq.idx], rq.phase, fault, kFaultWaitTma, abort))
           return false;
-        if (!mbar_wait(&sm.k_full[ks], (c.g / kKStages) & 1, fault, kFaultWaitTma, abort))
-          return false;
+        if (!mbar_wait(&sm.k_full[rk.idx], rk.phase, fault, kFaultWaitTma, abort)) return false;
         tc_fence_after();
+        const uint64_t dq = dq0 + rq.idx * qslot16, dk = dk0 + rk.idx * kSlot16;
+        const uint32_t ts = tbase + rs.idx * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t ad = sdesc_sw128(smem_u32(q_addr(qb, kk >> 2)) + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(smem_u32(sm.k[ks][kk >> 2]) + (kk & 3) * 32, 16, 1024);
-          mma_ss(tbase + b * 128, ad, bd, idS, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * kHalf16 + (kk & 3) * 2;
+          mma_ss(ts, dq + off, dk + off, idS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&sm.qk_done[c.g % kSBuf]);
-        if (c.u == c.it.n - 1) mma_commit(&sm.q_empty[qb]);
+        mma_commit(&sm.qk_done[rs.idx]);
+        if (c.u == c.it.n - 1) {
+          mma_commit(&sm.q_empty[rq.idx]);
+          rq.next();
+        }
+        rk.next();
+        rs.next();
         return true;
       };
       auto issue_pv = [&](const Cursor& c) -> bool {
-        const int b = c.g % kSBuf, vs = c.g % kVStages;
         // A new item's first PV overwrites O: its previous epilogue must have read it.
-        if (c.u == 0 && c.k > 0 &&
-            !mbar_wait(&sm.o_free, (c.k - 1) & 1, fault, kFaultWaitSoftmax, abort))
-          return false;
-        if (!mbar_wait(&sm.p_full[b], (c.g / kSBuf) & 1, fault, kFaultWaitSoftmax, abort))
-          return false;
-        if (!mbar_wait(&sm.v_full[vs], (c.g / kVStages) & 1, fault, kFaultWaitTma, abort))
-          return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t bd = sdesc_sw128(smem_u32(sm.v[vs][0]) + kk * 2048, kTile, 1024);
-          const uint32_t pcol = b * 128 + (kk >> 2) * 64 + (kk & 3) * 8;
-          mma_ts(tbase + kColO, tbase + pcol, bd, idO, (c.u > 0 || kk > 0) ? 1u : 0u);
+        if (c.u == 0 && c.k > 0) {
+          if (!mbar_wait(&sm.o_free, ofree_phase, fault, kFaultWaitSoftmax, abort)) return false;
+          ofree_phase ^= 1u;
         }
-        mma_commit(&sm.pv_done[c.g % kPV]);
+        if (!mbar_wait(&sm.p_full[rp.idx], rp.phase, fault, kFaultWaitSoftmax, abort)) return false;
+        if (!mbar_wait(&sm.v_full[rv.idx], rv.phase, fault, kFaultWaitTma, abort)) return false;
+        tc_fence_after();
+        const uint64_t dv = dv0 + rv.idx * kSlot16;
+        const uint32_t tp = tbase + rp.idx * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tbase + kColO, tp + (kk >> 2) * 64 + (kk & 3) * 8, dv + kk * 128, idO,
+                 (c.u > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&sm.pv_done[rp.idx]);
+        rv.next();
+        rp.next();
         return true;
       };
       Cursor qc, pc;
