@@ -798,12 +798,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       const size_t part = ((size_t)(it.tail < 0 ? 0 : it.tail) * a.splits + it.split) * a.rows_part;
       const bool has = lt > 0.f;
       const float inv = has ? 1.f / lt : 0.f;
-#pragma unroll
-      for (int hh = 0; hh < kHalves; ++hh) {
-        const int half = wg * kHalves + hh;
-        float o[64];
-        tmem_ld64(lane_base + kColO + half * 64, o);
-        if (!active) continue;
+      auto store_half = [&](int half, const float* o) {
+        if (!active) return;
         if (nsplit == 1) {
           uint4* dst =
               reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * 128);
@@ -822,20 +818,38 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 64; c += 4) dst[c >> 2] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
         }
+      };
+      // O is released (the next item's first PV may overwrite it) as soon as
+      // this warp's columns are in registers, before the global stores.
+      {
+        float o[64];
+        tmem_ld64(lane_base + kColO + wg * kHalves * 64, o);
+        if (kHalves == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.o_free);
+        }
+        store_half(wg * kHalves, o);
       }
-      // O has been read: the next item's first PV may overwrite it.
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.o_free);
+      if (kHalves == 2) {
+        float o[64];
+        tmem_ld64(lane_base + kColO + 64, o);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.o_free);
+        store_half(1, o);
+      }
       g += it.n;
-      if (!active || wg != 0) continue;
       if (nsplit == 1) {
-        if (a.lse != nullptr) a.lse[orow] = has ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+        if (active && wg == 0 && a.lse != nullptr)
+          a.lse[orow] = has ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
         continue;
       }
+      if (active && wg == 0) {
+        a.part_ml[(part + row) * 2] = m_ref;
+        a.part_ml[(part + row) * 2 + 1] = lt;
+      }
       // The unit's splits are combined by merge_splits_kernel after this launch.
-      a.part_ml[(part + row) * 2] = m_ref;
-      a.part_ml[(part + row) * 2 + 1] = lt;
     }
   }
 
