@@ -49,7 +49,7 @@ constexpr int kMinSplitBlocks = 4;
 struct PrefillLayout {
   int W, max_tiles, cap, words;
   int whole_units, tail_units, splits, pps, rows_part, num_items;
-  size_t off_info, off_len, off_blocks, off_member, off_part_o, off_part_ml, total;
+  size_t off_info, off_len, off_blocks, off_member, off_part_o, off_part_ml, off_counter, total;
 };
 
 PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk, int max_seqlen_q) {
@@ -121,6 +121,8 @@ PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk, 
   off += up256(parts * L.rows_part * 128 * sizeof(float));
   L.off_part_ml = off;
   off += up256(parts * L.rows_part * 2 * sizeof(float));
+  L.off_counter = off;
+  off += 256;
   L.total = off;
   return L;
 }
@@ -250,6 +252,7 @@ msa_status_t msa_sparse_attention_fwd(
   u.union_blocks = reinterpret_cast<int32_t*>(ws + L.off_blocks);
   u.member = reinterpret_cast<uint32_t*>(ws + L.off_member);
   u.tile_info = reinterpret_cast<int32_t*>(ws + L.off_info);
+  u.item_counter = reinterpret_cast<int32_t*>(ws + L.off_counter);
   mark(0, stream);
   cudaError_t e = launch_build_union(u, stream);
   if (e != cudaSuccess) return MSA_CUDA_ERROR;
@@ -298,6 +301,7 @@ msa_status_t msa_sparse_attention_fwd(
   a.num_items = L.num_items;
   a.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
   a.part_ml = reinterpret_cast<float*>(ws + L.off_part_ml);
+  a.item_counter = u.item_counter;
   e = launch_prefill(a, stream);
   mark(2, stream);
   return from_cuda(e);

@@ -31,6 +31,7 @@ struct UnionArgs {
   int32_t* union_blocks;
   uint32_t* member;
   int32_t* tile_info;  // may be NULL
+  int32_t* item_counter;  // may be NULL: set to 0 (the attention kernel's work counter)
 };
 cudaError_t launch_build_union(const UnionArgs& a, cudaStream_t s);
 
@@ -105,7 +106,7 @@ struct PrefillArgs {
   const int32_t* tile_info;
   void* out;
   float* lse;
-  // Work items, walked by a persistent grid. Units are (query tile, KV head)
+  // Work items, handed out dynamically to a persistent grid. Units are (query tile, KV head)
   // pairs, head-major with the heaviest tiles first within a head. The first whole_units units are one item each and
   // write out/lse directly. Each remaining ("tail") unit is split into
   // `splits` items, item s taking union entries [s*pps, (s+1)*pps); a tail
@@ -120,6 +121,7 @@ struct PrefillArgs {
   int num_items;
   float* part_o;        // (tail_units*splits, rows_part, 128)
   float* part_ml;       // (tail_units*splits, rows_part, 2)
+  int* item_counter;    // items handed out beyond the first round; 0 at launch
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 int device_sm_count();

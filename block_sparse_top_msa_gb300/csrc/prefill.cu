@@ -35,6 +35,7 @@ namespace {
 constexpr int kF8Stages = 2;    // E4M3 staging ring (K and V bytes of one block)
 constexpr int kSBuf = 3;        // S/P buffers in TMEM: QK runs two blocks ahead of PV
 constexpr int kPV = 3;          // PV completion barriers (block g uses g % kPV)
+constexpr int kItemRing = 4;    // work-item indices handed from the scheduler warp to the roles
 static_assert(kPV == kSBuf, "the MMA issuer walks S buffers and PV barriers with one ring");
 constexpr int kTile = 16384;    // bytes of one 128-row x 128-byte swizzled tile
 constexpr float kRescaleLog2 = 8.0f;
@@ -69,7 +70,11 @@ struct Roles {
   static constexpr int kMmaWarp = kSoftmaxWarps + 1;
   static constexpr int kVProducerWarp = FP8 ? -1 : kSoftmaxWarps + 2;  // V (bf16 only)
   static constexpr int kConvWarp0 = kSoftmaxWarps + 2;              // E4M3 converters
-  static constexpr int kWarps = kSoftmaxWarps + (FP8 ? 6 : 3);
+  static constexpr int kSchedWarp = kSoftmaxWarps + (FP8 ? 6 : 3);  // hands out work items
+  static constexpr int kWarps = kSchedWarp + 1;
+  // Readers of the item ring: K producer, V producer (bf16), the MMA
+  // issuer's two cursors, every softmax warp, every converter warp.
+  static constexpr int kItemReaders = 1 + (FP8 ? 0 : 1) + 2 + kSoftmaxWarps + (FP8 ? 4 : 0);
   static constexpr int kThreads = kWarps * 32;
 };
 
@@ -97,6 +102,9 @@ struct __align__(1024) PrefillSmem {
   uint64_t pv_done[kPV];
   uint64_t o_free;
   uint64_t drain;
+  uint64_t item_full[kItemRing];
+  uint64_t item_empty[kItemRing];
+  int item_idx[kItemRing];
   uint32_t tmem_base;
   int abort;
   float xch[kXch];  // [slot][warpgroup][row] values exchanged between the softmax warpgroups
@@ -263,9 +271,6 @@ MSA_DEV Item item_at(const PrefillArgs& a, int i, int2 ti) {
   return it;
 }
 
-// Position in the CTA's stream of blocks: item index i (stride gridDim.x),
-// block u inside the item, ordinal k of the item among non-empty items, and
-// global block ordinal g.
 // Slot index and phase parity of a position in a ring of N slots, advanced
 // one step at a time (no divisions on the MMA issue path).
 template <int N>
@@ -280,36 +285,14 @@ struct RingPos {
   }
 };
 
+// Position in the CTA's stream of blocks: n items read from the item ring,
+// block u inside the current item, ordinal k of the item among non-empty
+// items, and global block ordinal g.
 struct Cursor {
-  int i, u, k, g;
+  int n, u, k, g;
   bool valid;
   Item it;
 };
-
-MSA_DEV void cursor_next(const PrefillArgs& a, Cursor& c) {
-  ++c.g;
-  ++c.u;
-  while (c.u >= c.it.n) {
-    c.i += gridDim.x;
-    if (c.i >= a.num_items) {
-      c.valid = false;
-      return;
-    }
-    c.it = item_at(a, c.i, item_tile_info(a, c.i));
-    c.u = 0;
-    if (c.it.n > 0) ++c.k;
-  }
-  c.valid = true;
-}
-
-MSA_DEV void cursor_begin(const PrefillArgs& a, Cursor& c) {
-  c.i = (int)blockIdx.x - (int)gridDim.x;
-  c.u = 0;
-  c.k = -1;
-  c.g = -1;
-  c.it.n = 0;
-  cursor_next(a, c);
-}
 
 template <bool FP8, bool STREAM>
 __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
@@ -349,6 +332,19 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   auto pv_wait = [&](int j) {
     return mbar_wait(&sm.pv_done[j % kPV], (j / kPV) & 1, fault, kFaultWaitMma, abort);
   };
+  // The n-th work item of this CTA (-1 once there are none left), published
+  // by the scheduler warp in slot n % kItemRing. A reader keeps the index and
+  // releases the slot at once (release_item, one arrival per reader), so the
+  // scheduler never waits on anyone's progress, only on their reads.
+  auto read_item = [&](int n, bool& okr) -> int {
+    if (!mbar_wait(&sm.item_full[n % kItemRing], (n / kItemRing) & 1, fault, kFaultWaitOther,
+                   abort)) {
+      okr = false;
+      return -1;
+    }
+    return *reinterpret_cast<volatile int*>(&sm.item_idx[n % kItemRing]);
+  };
+  auto release_item = [&](int n) { mbar_arrive(&sm.item_empty[n % kItemRing]); };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.num_qo_heads / a.num_kv_heads;
   const int W = a.tile_tokens;
@@ -380,6 +376,10 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     for (int s = 0; s < kPV; ++s) mbar_init(&sm.pv_done[s], 1);
     mbar_init(&sm.o_free, R::kSoftmaxWarps);
     mbar_init(&sm.drain, 1);
+    for (int s = 0; s < kItemRing; ++s) {
+      mbar_init(&sm.item_full[s], 1);
+      mbar_init(&sm.item_empty[s], R::kItemReaders);
+    }
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -413,7 +413,11 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       for (int s = 0; s < kF8Stages; ++s) last_8[s] = -1;
       bool ok = true;
       int g = 0, k = 0;  // blocks issued, non-empty items seen
-      for (int i = blockIdx.x; ok && i < a.num_items; i += gridDim.x) {
+      for (int ni = 0; ok; ++ni) {
+        const int i = read_item(ni, ok);
+        if (!ok) break;
+        release_item(ni);
+        if (i < 0) break;
         const Item it = item_at(a, i, item_tile_info(a, i));
         if (it.n == 0) continue;
         if (kq) {
@@ -556,32 +560,58 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         rp.next();
         return true;
       };
+      // Moves a cursor to the next block, reading new items from the ring as
+      // it passes item boundaries; false if a read gave up.
+      auto cursor_next = [&](Cursor& c) -> bool {
+        ++c.g;
+        ++c.u;
+        while (c.u >= c.it.n) {
+          bool okr = true;
+          const int i = read_item(c.n, okr);
+          if (!okr) return false;
+          release_item(c.n);
+          ++c.n;
+          if (i < 0) {
+            c.valid = false;
+            return true;
+          }
+          c.it = item_at(a, i, item_tile_info(a, i));
+          c.u = 0;
+          if (c.it.n > 0) ++c.k;
+        }
+        c.valid = true;
+        return true;
+      };
       Cursor qc, pc;
-      cursor_begin(a, qc);
-      cursor_begin(a, pc);
-      for (int j = 0; ok && j < 2 && qc.valid; ++j) {
-        ok = issue_qk(qc);
-        cursor_next(a, qc);
-      }
+      qc.n = pc.n = 0;
+      qc.u = pc.u = 0;
+      qc.k = pc.k = -1;
+      qc.g = pc.g = -1;
+      qc.it.n = pc.it.n = 0;
+      ok = cursor_next(qc) && cursor_next(pc);
+      for (int j = 0; ok && j < 2 && qc.valid; ++j) ok = issue_qk(qc) && cursor_next(qc);
       while (ok && pc.valid) {
         if (qc.valid) {
-          ok = issue_qk(qc);
-          cursor_next(a, qc);
+          ok = issue_qk(qc) && cursor_next(qc);
           if (!ok) break;
         }
-        ok = issue_pv(pc);
-        cursor_next(a, pc);
+        ok = issue_pv(pc) && cursor_next(pc);
       }
       // Nothing may be in flight when TMEM is released.
       mma_commit(&sm.drain);
       mbar_wait(&sm.drain, 0, fault, kFaultWaitMma);
     }
-  } else if (FP8 && warp >= R::kConvWarp0) {
+  } else if (FP8 && warp >= R::kConvWarp0 && warp < R::kConvWarp0 + 4) {
     // ------------------------------------------------------------ E4M3 -> bf16
     const int ct = tid - R::kConvWarp0 * 32;
     int g = 0;
     bool ok = true;
-    for (int i = blockIdx.x; ok && i < a.num_items; i += gridDim.x) {
+    for (int ni = 0; ok; ++ni) {
+      const int i = read_item(ni, ok);
+      if (!ok) break;
+      __syncwarp();
+      if (lane == 0) release_item(ni);
+      if (i < 0) break;
       const Item it = item_at(a, i, item_tile_info(a, i));
       for (int u = 0; u < it.n; ++u, ++g) {
         const int s8 = g % kF8Stages, ks = g % kKStages, vs = g % kVStages;
@@ -605,6 +635,35 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
           mbar_arrive(&sm.v_full[vs]);
           mbar_arrive(&sm.f8_empty[s8]);
         }
+      }
+    }
+  } else if (warp == R::kSchedWarp) {
+    // ------------------------------------------------------------ scheduler
+    // Items are handed out dynamically: item blockIdx.x first, then whatever
+    // the launch-wide counter gives (in increasing order, heaviest first), so
+    // SMs that run faster take more. Items with nothing to do are skipped,
+    // except a tile's first split when the tile has no usable block (its
+    // rows are written as empty).
+    if (lane == 0) {
+      int next = blockIdx.x;
+      for (int n = 0;; ++n) {
+        const int slot = n % kItemRing;
+        if (n >= kItemRing &&
+            !mbar_wait(&sm.item_empty[slot], ((n / kItemRing) - 1) & 1, fault, kFaultWaitOther, abort))
+          break;
+        int i = -1;
+        while (next < a.num_items) {
+          const int cand = next;
+          next = (int)gridDim.x + atomicAdd(a.item_counter, 1);
+          const Item it = item_at(a, cand, item_tile_info(a, cand));
+          if (it.t0 >= 0 && (it.n > 0 || (it.split == 0 && it.n_union == 0))) {
+            i = cand;
+            break;
+          }
+        }
+        sm.item_idx[slot] = i;
+        mbar_arrive(&sm.item_full[slot]);
+        if (i < 0) break;
       }
     }
   } else if (warp < R::kSoftmaxWarps) {
@@ -631,12 +690,29 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       ++xi;
       return slot[(1 - wg) * 128 + row];
     };
-    int i = blockIdx.x;
-    int2 nti = i < a.num_items ? item_tile_info(a, i) : make_int2(-1, 0);
-    for (; ok && i < a.num_items; i += gridDim.x) {
-      const Item it = item_at(a, i, nti);
-      // The next item's tile is fetched while this one runs.
-      if (i + (int)gridDim.x < a.num_items) nti = item_tile_info(a, i + gridDim.x);
+    // Item indices are read one item ahead, so the next tile's metadata loads
+    // while this one runs. Waiting for item n + 1 at the start of item n
+    // cannot stall on this warp's own progress: the scheduler only needs
+    // item n + 1 - kItemRing to have been read by everyone, and every other
+    // reader is at least at item n - 1. Both warps of a pair agree on the
+    // outcome before going on (they meet at paired barriers below).
+    int ni = 0;
+    auto take = [&](bool& okr) -> int {
+      const int idx = read_item(ni, okr);
+      __syncwarp();
+      if (okr && lane == 0) release_item(ni);
+      ++ni;
+      return idx;
+    };
+    int inext = take(ok);
+    if (NW == 2) ok = pair_barrier_and(q4, ok);
+    int2 nti = inext >= 0 ? item_tile_info(a, inext) : make_int2(-1, 0);
+    while (ok && inext >= 0) {
+      const Item it = item_at(a, inext, nti);
+      inext = take(ok);
+      if (NW == 2) ok = pair_barrier_and(q4, ok);
+      if (!ok) break;
+      if (inext >= 0) nti = item_tile_info(a, inext);
       if (it.t0 < 0) continue;
       const int nw = min(W, it.seq_q0 + it.lq - it.t0);
       const bool active = row < W * G && w < nw;

@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(kUnionThreads)
   __shared__ int s_ulen;
 
   grid_dependents_launch();
+  if (a.item_counter != nullptr && tile == 0 && h == 0 && tid == 0) *a.item_counter = 0;
   int b = 0, t0 = 0;
   const bool live = locate_tile(a.cu_q, a.batch, a.tile_tokens, tile, scratch, &b, &t0);
   const size_t base = (size_t)h * a.max_tiles + tile;
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(1024) build_union_small_kernel(UnionArgs a) {
   __shared__ int s_ulen;
 
   grid_dependents_launch();
+  if (a.item_counter != nullptr && tile == 0 && h == 0 && tid == 0) *a.item_counter = 0;
   int b = 0, t0 = 0;
   const bool live = locate_tile(a.cu_q, a.batch, a.tile_tokens, tile, scratch, &b, &t0);
   const size_t base = (size_t)h * a.max_tiles + tile;
