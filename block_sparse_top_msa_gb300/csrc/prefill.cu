@@ -35,7 +35,8 @@ namespace {
 constexpr int kF8Stages = 2;    // E4M3 staging ring (K and V bytes of one block)
 constexpr int kSBuf = 3;        // S/P buffers in TMEM: QK runs two blocks ahead of PV
 constexpr int kPV = 3;          // PV completion barriers (block g uses g % kPV)
-constexpr int kItemRing = 4;    // work-item indices handed from the scheduler warp to the roles
+constexpr int kItemRing = 4;    // work items handed from the K producer to the other roles
+constexpr int kClaimAhead = 4;  // the K producer claims its next item this many blocks early
 static_assert(kPV == kSBuf, "the MMA issuer walks S buffers and PV barriers with one ring");
 constexpr int kTile = 16384;    // bytes of one 128-row x 128-byte swizzled tile
 constexpr float kRescaleLog2 = 8.0f;
@@ -58,6 +59,14 @@ constexpr uint32_t kColO = 384;
 // issued before it) has completed: S_g is readable and the K slot of block g
 // is free. pv_done[g % 3] likewise for PV(g): O holds block g and its V slot
 // is free. One commit per MMA group keeps the issuing thread's overhead low.
+// One work item: a (query tile, KV head, split) triple and its slice of the
+// tile's union list. Every role derives the same items in the same order.
+struct Item {
+  int tile, h, split, t0, b, n_union, p_begin, n;
+  int tail;                 // index among the split (tail) units, or -1 for a whole unit
+  int seq_q0, lq, lk, kv0;  // the tile's sequence (valid when t0 >= 0)
+};
+
 // Warp roles. The softmax runs in kSoftmaxWG warpgroups; with two, warps q
 // and q + 4 share TMEM lanes 32q..32q+31 and split each S row by columns
 // (0..63 and 64..127), exchanging their partial row maxima every block. The
@@ -70,11 +79,10 @@ struct Roles {
   static constexpr int kMmaWarp = kSoftmaxWarps + 1;
   static constexpr int kVProducerWarp = FP8 ? -1 : kSoftmaxWarps + 2;  // V (bf16 only)
   static constexpr int kConvWarp0 = kSoftmaxWarps + 2;              // E4M3 converters
-  static constexpr int kSchedWarp = kSoftmaxWarps + (FP8 ? 6 : 3);  // hands out work items
-  static constexpr int kWarps = kSchedWarp + 1;
-  // Readers of the item ring: K producer, V producer (bf16), the MMA
-  // issuer's two cursors, every softmax warp, every converter warp.
-  static constexpr int kItemReaders = 1 + (FP8 ? 0 : 1) + 2 + kSoftmaxWarps + (FP8 ? 4 : 0);
+  static constexpr int kWarps = kSoftmaxWarps + (FP8 ? 6 : 3);
+  // Readers of the item ring (the K producer writes it): V producer (bf16),
+  // the MMA issuer's two cursors, every softmax warp, every converter warp.
+  static constexpr int kItemReaders = (FP8 ? 0 : 1) + 2 + kSoftmaxWarps + (FP8 ? 4 : 0);
   static constexpr int kThreads = kWarps * 32;
 };
 
@@ -105,6 +113,7 @@ struct __align__(1024) PrefillSmem {
   uint64_t item_full[kItemRing];
   uint64_t item_empty[kItemRing];
   int item_idx[kItemRing];
+  Item item_ring[kItemRing];
   uint32_t tmem_base;
   int abort;
   float xch[kXch];  // [slot][warpgroup][row] values exchanged between the softmax warpgroups
@@ -215,13 +224,6 @@ MSA_DEV void convert_tile(const uint8_t* src, uint8_t* dst_half0, int t) {
   }
 }
 
-// One work item: a (query tile, KV head, split) triple and its slice of the
-// tile's union list. Every role derives the same items in the same order.
-struct Item {
-  int tile, h, split, t0, b, n_union, p_begin, n;
-  int tail;                 // index among the split (tail) units, or -1 for a whole unit
-  int seq_q0, lq, lk, kv0;  // the tile's sequence (valid when t0 >= 0)
-};
 
 // The (t0, b) pair of item i's tile, the one field that needs a load before
 // the rest can be fetched (and that the softmax warps fetch one item ahead).
@@ -332,17 +334,19 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   auto pv_wait = [&](int j) {
     return mbar_wait(&sm.pv_done[j % kPV], (j / kPV) & 1, fault, kFaultWaitMma, abort);
   };
-  // The n-th work item of this CTA (-1 once there are none left), published
-  // by the scheduler warp in slot n % kItemRing. A reader keeps the index and
-  // releases the slot at once (release_item, one arrival per reader), so the
-  // scheduler never waits on anyone's progress, only on their reads.
-  auto read_item = [&](int n, bool& okr) -> int {
-    if (!mbar_wait(&sm.item_full[n % kItemRing], (n / kItemRing) & 1, fault, kFaultWaitOther,
-                   abort)) {
+  // The n-th work item of this CTA (index -1 once there are none left) and
+  // its fields, published by the K producer in slot n % kItemRing. A reader
+  // copies the item and releases the slot at once (release_item, one arrival
+  // per reader), so the publisher only ever waits on reads, not on progress.
+  auto read_item = [&](int n, bool& okr, Item& it) -> int {
+    const int slot = n % kItemRing;
+    if (!mbar_wait(&sm.item_full[slot], (n / kItemRing) & 1, fault, kFaultWaitOther, abort)) {
       okr = false;
       return -1;
     }
-    return *reinterpret_cast<volatile int*>(&sm.item_idx[n % kItemRing]);
+    const int idx = *reinterpret_cast<volatile int*>(&sm.item_idx[slot]);
+    if (idx >= 0) it = sm.item_ring[slot];
+    return idx;
   };
   auto release_item = [&](int n) { mbar_arrive(&sm.item_empty[n % kItemRing]); };
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -413,12 +417,43 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       for (int s = 0; s < kF8Stages; ++s) last_8[s] = -1;
       bool ok = true;
       int g = 0, k = 0;  // blocks issued, non-empty items seen
+      // The K producer hands out the work: its first item is blockIdx.x, each
+      // later one comes from the launch-wide counter (in increasing order,
+      // heaviest first), claimed kClaimAhead blocks before the current item
+      // ends, so SMs that run faster take more items. Items with nothing to do
+      // are skipped, except a tile's first split when the tile has no usable
+      // block (its rows are written as empty by the softmax warps).
+      int claim = blockIdx.x;
       for (int ni = 0; ok; ++ni) {
-        const int i = read_item(ni, ok);
-        if (!ok) break;
-        release_item(ni);
-        if (i < 0) break;
-        const Item it = item_at(a, i, item_tile_info(a, i));
+        Item it{};
+        int i = -1;
+        if (kq) {
+          while (claim < a.num_items) {
+            const int cand = claim;
+            it = item_at(a, cand, item_tile_info(a, cand));
+            if (it.t0 >= 0 && (it.n > 0 || (it.split == 0 && it.n_union == 0))) {
+              i = cand;
+              break;
+            }
+            claim = (int)gridDim.x + atomicAdd(a.item_counter, 1);
+          }
+          const int slot = ni % kItemRing;
+          if (ni >= kItemRing && !mbar_wait(&sm.item_empty[slot], ((ni / kItemRing) - 1) & 1, fault,
+                                            kFaultWaitOther, abort)) {
+            ok = false;
+            break;
+          }
+          sm.item_idx[slot] = i;
+          if (i >= 0) sm.item_ring[slot] = it;
+          mbar_arrive(&sm.item_full[slot]);
+          if (i < 0) break;
+          if (it.n <= kClaimAhead) claim = (int)gridDim.x + atomicAdd(a.item_counter, 1);
+        } else {
+          i = read_item(ni, ok, it);
+          if (!ok) break;
+          release_item(ni);
+          if (i < 0) break;
+        }
         if (it.n == 0) continue;
         if (kq) {
           const int qb = k % kQBuf;
@@ -434,6 +469,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         const int32_t* ulist =
             a.union_blocks + ((size_t)it.h * a.max_tiles + it.tile) * a.cap + it.p_begin;
         for (int u = 0; u < it.n; ++u, ++g) {
+          if (kq && it.n > kClaimAhead && u == it.n - kClaimAhead)
+            claim = (int)gridDim.x + atomicAdd(a.item_counter, 1);
           const int blk = ulist[u];
           int page = 0;
           if (a.paged) {
@@ -567,7 +604,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         ++c.u;
         while (c.u >= c.it.n) {
           bool okr = true;
-          const int i = read_item(c.n, okr);
+          const int i = read_item(c.n, okr, c.it);
           if (!okr) return false;
           release_item(c.n);
           ++c.n;
@@ -575,7 +612,6 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
             c.valid = false;
             return true;
           }
-          c.it = item_at(a, i, item_tile_info(a, i));
           c.u = 0;
           if (c.it.n > 0) ++c.k;
         }
@@ -607,12 +643,12 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     int g = 0;
     bool ok = true;
     for (int ni = 0; ok; ++ni) {
-      const int i = read_item(ni, ok);
+      Item it{};
+      const int i = read_item(ni, ok, it);
       if (!ok) break;
       __syncwarp();
       if (lane == 0) release_item(ni);
       if (i < 0) break;
-      const Item it = item_at(a, i, item_tile_info(a, i));
       for (int u = 0; u < it.n; ++u, ++g) {
         const int s8 = g % kF8Stages, ks = g % kKStages, vs = g % kVStages;
         if (!mbar_wait(&sm.f8_full[s8], (g / kF8Stages) & 1, fault, kFaultWaitTma, abort) ||
@@ -635,35 +671,6 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
           mbar_arrive(&sm.v_full[vs]);
           mbar_arrive(&sm.f8_empty[s8]);
         }
-      }
-    }
-  } else if (warp == R::kSchedWarp) {
-    // ------------------------------------------------------------ scheduler
-    // Items are handed out dynamically: item blockIdx.x first, then whatever
-    // the launch-wide counter gives (in increasing order, heaviest first), so
-    // SMs that run faster take more. Items with nothing to do are skipped,
-    // except a tile's first split when the tile has no usable block (its
-    // rows are written as empty).
-    if (lane == 0) {
-      int next = blockIdx.x;
-      for (int n = 0;; ++n) {
-        const int slot = n % kItemRing;
-        if (n >= kItemRing &&
-            !mbar_wait(&sm.item_empty[slot], ((n / kItemRing) - 1) & 1, fault, kFaultWaitOther, abort))
-          break;
-        int i = -1;
-        while (next < a.num_items) {
-          const int cand = next;
-          next = (int)gridDim.x + atomicAdd(a.item_counter, 1);
-          const Item it = item_at(a, cand, item_tile_info(a, cand));
-          if (it.t0 >= 0 && (it.n > 0 || (it.split == 0 && it.n_union == 0))) {
-            i = cand;
-            break;
-          }
-        }
-        sm.item_idx[slot] = i;
-        mbar_arrive(&sm.item_full[slot]);
-        if (i < 0) break;
       }
     }
   } else if (warp < R::kSoftmaxWarps) {
@@ -690,29 +697,15 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       ++xi;
       return slot[(1 - wg) * 128 + row];
     };
-    // Item indices are read one item ahead, so the next tile's metadata loads
-    // while this one runs. Waiting for item n + 1 at the start of item n
-    // cannot stall on this warp's own progress: the scheduler only needs
-    // item n + 1 - kItemRing to have been read by everyone, and every other
-    // reader is at least at item n - 1. Both warps of a pair agree on the
-    // outcome before going on (they meet at paired barriers below).
-    int ni = 0;
-    auto take = [&](bool& okr) -> int {
-      const int idx = read_item(ni, okr);
+    // Both warps of a pair agree on each read's outcome before going on
+    // (they meet at paired barriers below).
+    for (int ni = 0;; ++ni) {
+      Item it{};
+      const int cur = read_item(ni, ok, it);
       __syncwarp();
-      if (okr && lane == 0) release_item(ni);
-      ++ni;
-      return idx;
-    };
-    int inext = take(ok);
-    if (NW == 2) ok = pair_barrier_and(q4, ok);
-    int2 nti = inext >= 0 ? item_tile_info(a, inext) : make_int2(-1, 0);
-    while (ok && inext >= 0) {
-      const Item it = item_at(a, inext, nti);
-      inext = take(ok);
+      if (ok && lane == 0) release_item(ni);
       if (NW == 2) ok = pair_barrier_and(q4, ok);
-      if (!ok) break;
-      if (inext >= 0) nti = item_tile_info(a, inext);
+      if (!ok || cur < 0) break;
       if (it.t0 < 0) continue;
       const int nw = min(W, it.seq_q0 + it.lq - it.t0);
       const bool active = row < W * G && w < nw;
