@@ -83,7 +83,7 @@ def barrier(world):
 # build that was captured; otherwise the roofline's "traffic" is null.
 TRAFFIC_SOURCES = ("prefill.cu", "common.cuh", "tmem_wide.cuh", "internal.h", "tmap.h", "api.cu",
                    "union.cu", "tile_map.cuh")
-TRAFFIC_MEASURED = {"fingerprint": "d1dbcccb215b3471", "bytes_per_launch": 2.433e9,
+TRAFFIC_MEASURED = {"fingerprint": "34f8e2c00224d9a0", "bytes_per_launch": 2.425e9,
                     "profile": "profiles/prefill_kernel_flat_varlen_2x32768_traffic.md"}
 
 
@@ -540,6 +540,9 @@ def main():
                     help="profiling case: prefill only, 1 x 8192 tokens, 64/8 heads, top-16")
     ap.add_argument("--profile-decode", type=int, default=0, metavar="SQ",
                     help="profiling case: paged decode only, 64 requests, seqlen_q SQ")
+    ap.add_argument("--profile-two-stage", action="store_true",
+                    help="profiling case: proxy score, top-k and attention of the two-stage "
+                         "workload only")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -558,6 +561,10 @@ def main():
         r = bench_decode(msa, device, flush, small=True, sqs=(args.profile_decode,),
                          reps=args.steps)
         print(json.dumps({"profile_decode": r}))
+        return 0
+    if args.profile_two_stage:
+        flush = l2_flush_buffer(device)
+        print(json.dumps({"profile_two_stage": bench_two_stage(msa, device, flush)}))
         return 0
     if args.profile_small:
         args.no_secondary = args.no_cpu_baseline = True
