@@ -109,10 +109,13 @@ def test_union_paged_lengths(msa):
 
 
 # ---------------------------------------------------------------- top-k
-@pytest.mark.parametrize("topk,hs,hkv", [(16, 1, 4), (1, 1, 2), (5, 3, 3), (33, 1, 1), (64, 2, 2)])
-def test_topk_bit_exact(msa, topk, hs, hkv):
-    rng = np.random.default_rng(topk + hs)
-    T, n = 97, 1000
+@pytest.mark.parametrize("topk,hs,hkv,n", [(16, 1, 4, 1000), (1, 1, 2, 1000), (5, 3, 3, 1000),
+                                           (33, 1, 1, 1000), (64, 2, 2, 1000),
+                                           (16, 2, 2, 1003),  # unaligned rows: scalar loads
+                                           (8, 1, 1, 37)])    # fewer queries than a CTA
+def test_topk_bit_exact(msa, topk, hs, hkv, n):
+    rng = np.random.default_rng(topk + hs + n)
+    T = 97
     s = rng.integers(-20, 20, size=(hs, T, n)).astype(np.float32) / 4  # many ties
     s[rng.random(s.shape) < 0.1] = -np.inf
     s[rng.random(s.shape) < 0.02] = np.nan
