@@ -232,6 +232,12 @@ DECODE_CASES = [
     ("sq3_g4", 3, [1500, 257, 10], 8, 2, 5),
     ("sq1_mha", 1, [600, 128], 4, 4, 3),
     ("sq4_g16_topk64", 4, [20000], 16, 1, 64),
+    # multi-token decode: 5..32 query tokens per request (one or several tiles)
+    ("sq5_g16", 5, [3000, 400], 32, 2, 16),
+    ("sq8_g16", 8, [4000, 130], 32, 2, 16),
+    ("sq8_g8", 8, [2500, 900, 260], 16, 2, 16),
+    ("sq16_g16", 16, [5000], 32, 2, 16),
+    ("sq32_g16", 32, [6000, 1000], 32, 2, 16),
 ]
 
 
@@ -262,6 +268,65 @@ def test_decode_parity(msa, case):
     out, lse = _run_prefill(msa, inp, max_seqlen_q=sq)
     ref_out, ref_lse = _oracle(inp)
     check_attention(out, lse, ref_out, ref_lse, label=name)
+
+
+def _decode_inputs(g, seqused, sq, hq, hkv, topk, npg_extra=3):
+    cu_q = torch.arange(0, len(seqused) * sq + 1, sq, dtype=torch.int32)
+    pages = [(n + 127) // 128 for n in seqused]
+    npg = sum(pages) + npg_extra
+    perm = torch.randperm(npg, generator=g).to(torch.int32)
+    pt = torch.zeros(len(seqused), max(pages), dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(pages):
+        pt[b, :n] = perm[off:off + n]
+        off += n
+    k = torch.randn(npg, hkv, 128, 128, generator=g).to(torch.bfloat16)
+    v = torch.randn(npg, hkv, 128, 128, generator=g).to(torch.bfloat16)
+    q = torch.randn(len(seqused) * sq, hq, 128, generator=g).to(torch.bfloat16)
+    q2k = workloads.select_blocks(workloads.query_positions(cu_q, seqused), hkv, topk, g)
+    return dict(q=q, k=k, v=v, q2k_indices=q2k, cu_seqlens_q=cu_q, page_table=pt,
+                seqused_k=torch.tensor(seqused, dtype=torch.int32))
+
+
+def test_decode_graph_replay(msa):
+    """The forward is captured once into a CUDA graph with caller-owned out, lse
+    and workspace and explicit sizes (no allocation, no host read-back); each
+    replay computes on whatever inputs were copied into the captured buffers."""
+    seqused, sq, hq, hkv, topk = [3000, 900, 129], 1, 32, 2, 16
+    g = torch.Generator().manual_seed(7)
+    host = _decode_inputs(g, seqused, sq, hq, hkv, topk)
+    dev = to_dev(host, DEV)
+    out = torch.empty_like(dev["q"])
+    lse = torch.empty(dev["q"].shape[:2], dtype=torch.float32, device=DEV)
+    need = msa.msa_sparse_attention_workspace_size(len(seqused), dev["q"].shape[0], hq, hkv, 128,
+                                                   topk, sq, True)
+    ws = torch.empty(need, dtype=torch.uint8, device=DEV)
+
+    def call():
+        msa.msa_sparse_attention_fwd(dev["q"], dev["k"], dev["v"], dev["q2k_indices"],
+                                     dev["cu_seqlens_q"], None, causal=True,
+                                     page_table=dev["page_table"], seqused_k=dev["seqused_k"],
+                                     max_seqlen_q=sq, out=out, lse=lse, workspace=ws)
+
+    call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            call()
+    torch.cuda.synchronize()
+    for trial in range(2):
+        new = _decode_inputs(torch.Generator().manual_seed(100 + trial), seqused, sq, hq, hkv,
+                             topk)
+        for key in ("q", "k", "v", "q2k_indices", "page_table"):
+            dev[key].copy_(new[key])
+        graph.replay()
+        torch.cuda.synchronize()
+        fault_clear(msa)
+        ref_out, ref_lse = _oracle(new)
+        check_attention(out, lse, ref_out, ref_lse, label=f"graph_replay_{trial}")
 
 
 def test_decode_deterministic(msa):
