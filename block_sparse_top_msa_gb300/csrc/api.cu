@@ -215,8 +215,10 @@ msa_status_t msa_sparse_attention_fwd(
       (workspace && !aligned(workspace, 256)))
     return MSA_INVALID_ARG;
   if (head_dim != 128) return MSA_UNSUPPORTED;
-  if (q_dtype != MSA_BF16) return MSA_UNSUPPORTED;
-  if (kv_dtype != MSA_BF16 && kv_dtype != MSA_FP8_E4M3) return MSA_UNSUPPORTED;
+  // bf16 q with bf16 or E4M3 K/V, or fp16 q with fp16 K/V.
+  if (q_dtype == MSA_FP16 ? kv_dtype != MSA_FP16
+                          : (q_dtype != MSA_BF16 || (kv_dtype != MSA_BF16 && kv_dtype != MSA_FP8_E4M3)))
+    return MSA_UNSUPPORTED;
   if (topk < 1 || topk > kMaxTopk) return MSA_UNSUPPORTED;
   const int G = num_qo_heads / num_kv_heads;
   if (G > 128) return MSA_UNSUPPORTED;
@@ -271,6 +273,7 @@ msa_status_t msa_sparse_attention_fwd(
   if (!ok) return MSA_CUDA_ERROR;
   a.paged = paged ? 1 : 0;
   a.kv_fp8 = esize == 1 ? 1 : 0;
+  a.f16 = q_dtype == MSA_FP16 ? 1 : 0;
   a.cu_q = cu_seqlens_q;
   a.cu_k = cu_seqlens_k;
   a.page_table = page_table;

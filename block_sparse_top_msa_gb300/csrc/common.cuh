@@ -180,6 +180,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
          ((uint32_t)(N >> 3) << 17)         // N / 8
          | ((uint32_t)(M >> 4) << 24);      // M / 16
 }
+// The same with A and B both f16 (format code 0) when f16, else both bf16.
+__host__ __device__ constexpr uint32_t idesc_16bit_f32(int M, int N, bool a_mn, bool b_mn,
+                                                       bool f16) {
+  return f16 ? (idesc_bf16_f32(M, N, a_mn, b_mn) & ~((1u << 7) | (1u << 10)))
+             : idesc_bf16_f32(M, N, a_mn, b_mn);
+}
 
 // 32 lanes x 32 bits x 16 columns: thread i of the warp reads lane (base + i),
 // columns [col, col + 16). Load and wait in one statement, so the registers are
@@ -232,6 +238,15 @@ MSA_DEV void tmem_st16(uint32_t taddr, const uint32_t* r) {
 MSA_DEV uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&p);
+}
+MSA_DEV uint32_t pack_f16x2(float lo, float hi) {
+  __half2 p = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+// Two floats as a packed pair of the 16-bit type of the operands (lo first).
+template <bool F16>
+MSA_DEV uint32_t pack_x2(float lo, float hi) {
+  return F16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
 
 // Byte offset of the 16-byte chunk `c16` (0..7) of row `row` inside a

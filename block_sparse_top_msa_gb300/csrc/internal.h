@@ -84,6 +84,7 @@ struct PrefillArgs {
   CUtensorMap tmap_v;
   int paged;
   int kv_fp8;
+  int f16;              // q, k, v and out are fp16 (else bf16; E4M3 K/V only with bf16)
   const int32_t* cu_q;
   const int32_t* cu_k;
   const int32_t* page_table;

@@ -177,9 +177,10 @@ MSA_DEV void update_max(bool mem, float mx, float scale_log2, float& m_ref, floa
   }
 }
 
-// P = 2^(s * scale_log2 + neg_m) for N columns, packed to bf16 pairs and
-// stored to TMEM at pcol (N/2 columns); the fp32 values are summed into acc.
-template <int N>
+// P = 2^(s * scale_log2 + neg_m) for N columns, packed to 16-bit pairs (the
+// type of V) and stored to TMEM at pcol (N/2 columns); the fp32 values are
+// summed into acc. P <= 2^8, well inside the f16 range.
+template <int N, bool F16 = false>
 MSA_DEV void exp_pack_store(const float* sv, float2 sc2, float neg_m, float2& acc, uint32_t pcol) {
   uint32_t pk[N / 2];
   const float2 nm2 = make_float2(neg_m, neg_m);
@@ -188,7 +189,7 @@ MSA_DEV void exp_pack_store(const float* sv, float2 sc2, float neg_m, float2& ac
     const float2 x = __ffma2_rn(make_float2(sv[c], sv[c + 1]), sc2, nm2);
     const float p0 = ex2(x.x), p1 = ex2(x.y);
     acc = __fadd2_rn(acc, make_float2(p0, p1));
-    pk[c >> 1] = pack_bf16x2(p0, p1);
+    pk[c >> 1] = pack_x2<F16>(p0, p1);
   }
   if (N == 64) tmem_st32(pcol, pk);
 }
@@ -296,9 +297,10 @@ struct Cursor {
   Item it;
 };
 
-template <bool FP8, bool STREAM>
+template <bool FP8, bool STREAM, bool F16>
 __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillArgs a) {
+  static_assert(!(FP8 && F16), "E4M3 K/V are upconverted to bf16");
   using R = Roles<FP8>;
   using Smem = PrefillSmem<FP8, STREAM>;
   constexpr int kQBuf = Smem::kQBuf;
@@ -538,8 +540,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
     // Walks the block stream twice: QK runs two blocks ahead of PV, across
     // item boundaries, so the softmax of block g overlaps PV(g-1) and QK(g+1).
     if (lane == 0) {
-      const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
-      const uint32_t idO = idesc_bf16_f32(128, 128, false, true);
+      const uint32_t idS = idesc_16bit_f32(128, 128, false, false, F16);
+      const uint32_t idO = idesc_16bit_f32(128, 128, false, true, F16);
       bool ok = true;
       // Descriptors of slot 0; a slot or K step only moves the start-address
       // field (16-byte units), so the issue path adds constants.
@@ -787,7 +789,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
             update_max(mem, mx, a.scale_log2, m_ref, l, alpha, rescale);
             // Non-member rows use -inf as their offset, so every P entry is 0.
             const float neg_m = mem ? -m_ref : -INFINITY;
-            exp_pack_store<64>(sv, sc2, neg_m, acc, gcol);
+            exp_pack_store<64, F16>(sv, sc2, neg_m, acc, gcol);
           } else {
             // QK(gg) overwrote this buffer: P must be rewritten (zeros) every block.
             uint32_t pk[32];
@@ -821,7 +823,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
                   if (half * 64 + c > lim) sv[c] = -INFINITY;
               }
               // Written over columns of this half that were just read.
-              exp_pack_store<64>(sv, sc2, neg_m, acc, scol + half * 64);
+              exp_pack_store<64, F16>(sv, sc2, neg_m, acc, scol + half * 64);
             }
           } else {
             uint32_t pk[32];
@@ -876,10 +878,10 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
           for (int c = 0; c < 64; c += 8) {
             uint4 v4 = make_uint4(0u, 0u, 0u, 0u);
             if (has)
-              v4 = make_uint4(pack_bf16x2(o[c] * inv, o[c + 1] * inv),
-                              pack_bf16x2(o[c + 2] * inv, o[c + 3] * inv),
-                              pack_bf16x2(o[c + 4] * inv, o[c + 5] * inv),
-                              pack_bf16x2(o[c + 6] * inv, o[c + 7] * inv));
+              v4 = make_uint4(pack_x2<F16>(o[c] * inv, o[c + 1] * inv),
+                              pack_x2<F16>(o[c + 2] * inv, o[c + 3] * inv),
+                              pack_x2<F16>(o[c + 4] * inv, o[c + 5] * inv),
+                              pack_x2<F16>(o[c + 6] * inv, o[c + 7] * inv));
             dst[(half * 64 + c) >> 3] = v4;
           }
         } else {
@@ -996,12 +998,13 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const __grid_constant
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const size_t orow = (size_t)(t0 + w) * a.num_qo_heads + (size_t)h * G + gh;
   uint2* dst = reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * 128) + lane;
-  *dst = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  *dst = a.f16 ? make_uint2(pack_f16x2(acc.x * inv, acc.y * inv), pack_f16x2(acc.z * inv, acc.w * inv))
+               : make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
   if (lane == 0 && a.lse != nullptr)
     a.lse[orow] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
-template <bool FP8, bool STREAM>
+template <bool FP8, bool STREAM, bool F16>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   // Up to 1 KiB of slack for aligning the base, within the per-block limit
   // (the kernel checks that the slack it got covers its base's offset).
@@ -1012,13 +1015,13 @@ cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   size_t smem = sizeof(PrefillSmem<FP8, STREAM>) + 1024;
   if (smem > (size_t)optin) smem = (size_t)optin;
-  e = cudaFuncSetAttribute(prefill_kernel<FP8, STREAM>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  e = cudaFuncSetAttribute(prefill_kernel<FP8, STREAM, F16>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = a.num_items < device_sm_count() ? a.num_items : device_sm_count();
   if (grid <= 0) return cudaSuccess;
-  e = launch_dependent(prefill_kernel<FP8, STREAM>, dim3(grid), dim3(Roles<FP8>::kThreads), smem,
-                       s, a);
+  e = launch_dependent(prefill_kernel<FP8, STREAM, F16>, dim3(grid), dim3(Roles<FP8>::kThreads),
+                       smem, s, a);
   if (e != cudaSuccess || a.splits <= 1 || a.tail_units == 0) return e;
   const long long warps = (long long)a.tail_units * a.rows_part;
   return launch_dependent(merge_splits_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s,
@@ -1041,12 +1044,13 @@ int device_sm_count() {
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s) {
-  if (a.kv_fp8) return launch_t<true, false>(a, s);
+  if (a.kv_fp8) return launch_t<true, false, false>(a, s);
   // Split launches are the memory-bound, decode-sized ones; their Q slots
   // share a region when a tile has at most 64 rows (whole 8-row groups).
   const int rows = a.tile_tokens * (a.num_qo_heads / a.num_kv_heads);
   const bool stream = a.splits > 1 && a.tail_units > 0 && rows <= 64 && rows % 8 == 0;
-  return stream ? launch_t<false, true>(a, s) : launch_t<false, false>(a, s);
+  if (a.f16) return stream ? launch_t<false, true, true>(a, s) : launch_t<false, false, true>(a, s);
+  return stream ? launch_t<false, true, false>(a, s) : launch_t<false, false, false>(a, s);
 }
 
 }  // namespace msa

@@ -68,10 +68,11 @@ size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_he
  * tiles that each run one online softmax over the union of their tokens'
  * blocks; the union metadata is built into the workspace.
  *
- *   q            device, (Tq, Hq, d), q_dtype (MSA_BF16)
+ *   q            device, (Tq, Hq, d), q_dtype MSA_BF16 or MSA_FP16
  *   k, v         device; flat (Tk, Hkv, d) when page_table == NULL, else
- *                paged (num_pages, Hkv, BLK, d); kv_dtype MSA_BF16 or MSA_FP8_E4M3
- *                (E4M3 "fn", upconverted exactly in-kernel; needs bf16 q)
+ *                paged (num_pages, Hkv, BLK, d); kv_dtype: with bf16 q,
+ *                MSA_BF16 or MSA_FP8_E4M3 (E4M3 "fn", upconverted exactly
+ *                in-kernel); with fp16 q, MSA_FP16
  *   q2k_indices  device int32 (Hkv, Tq, topk); 1 <= topk <= 64
  *   cu_seqlens_q device int32 (B+1), cumulative query lengths
  *   cu_seqlens_k device int32 (B+1) for flat K/V; must be NULL when paged
@@ -94,7 +95,7 @@ size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_he
  * are given (paged length comes only from seqused_k, per the page's rule of
  * declining two possibly disagreeing length sources), when Hq % Hkv != 0, or
  * when a pointer is NULL or misaligned; MSA_UNSUPPORTED for head_dim != 128,
- * q not bf16, or topk outside [1, 64].
+ * a dtype pair other than those above, or topk outside [1, 64].
  */
 msa_status_t msa_sparse_attention_fwd(
     const void* q, msa_dtype_t q_dtype, const void* k, const void* v, msa_dtype_t kv_dtype,

@@ -105,7 +105,10 @@ def test_forward_argument_errors(L):
     assert fwd(L, total_k=0) == 1
     assert fwd(L, d=64) == 2                         # head_dim
     assert fwd(L, qdt=2) == 2                        # fp8 q
-    assert fwd(L, qdt=1) == 2                        # fp16 q: not built
+    assert fwd(L, qdt=1) == 2                        # fp16 q with bf16 K/V
+    assert fwd(L, qdt=0, kvdt=1) == 2                # bf16 q with fp16 K/V
+    assert fwd(L, qdt=1, kvdt=2) == 2                # fp16 q with E4M3 K/V
+    assert fwd(L, qdt=1, kvdt=1, ws_bytes=16) == 3   # fp16 q and K/V: accepted
     assert fwd(L, topk=0) == 2 and fwd(L, topk=65) == 2
     assert fwd(L, hq=256, hkv=1) == 2                # G > 128
     assert fwd(L, ws_bytes=16) == 3                  # workspace too small

@@ -31,8 +31,11 @@ def _prefill_inputs(lens_q, lens_k, hq, hkv, topk, seed, kv="bf16", first_prev=F
     g = torch.Generator().manual_seed(seed)
     d = 128
     tq, tk = sum(lens_q), sum(lens_k)
-    q = torch.randn(tq, hq, d, generator=g).to(torch.bfloat16)
-    if kv == "e4m3":
+    q = torch.randn(tq, hq, d, generator=g).to(torch.float16 if kv == "f16" else torch.bfloat16)
+    if kv == "f16":
+        k = torch.randn(tk, hkv, d, generator=g).to(torch.float16)
+        v = torch.randn(tk, hkv, d, generator=g).to(torch.float16)
+    elif kv == "e4m3":
         k = torch.randn(tk, hkv, d, generator=g).to(torch.float8_e4m3fn)
         v = torch.randn(tk, hkv, d, generator=g).to(torch.float8_e4m3fn)
     else:
@@ -142,6 +145,8 @@ PREFILL_CASES = [
     ("topk1", [300], [300], 8, 1, 1, "bf16", False),
     ("topk64", [1200], [1200], 8, 1, 64, "bf16", False),
     ("mha_topk16_wide_union", [700, 260], [700, 260], 2, 2, 16, "bf16", True),
+    ("f16_gqa8_varlen", [300, 517, 64], [300, 517, 900], 16, 2, 8, "f16", True),
+    ("f16_gqa4_split", [200], [200], 8, 2, 4, "f16", False),
 ]
 
 
@@ -270,7 +275,7 @@ def test_decode_parity(msa, case):
     check_attention(out, lse, ref_out, ref_lse, label=name)
 
 
-def _decode_inputs(g, seqused, sq, hq, hkv, topk, npg_extra=3):
+def _decode_inputs(g, seqused, sq, hq, hkv, topk, npg_extra=3, dtype=torch.bfloat16):
     cu_q = torch.arange(0, len(seqused) * sq + 1, sq, dtype=torch.int32)
     pages = [(n + 127) // 128 for n in seqused]
     npg = sum(pages) + npg_extra
@@ -280,9 +285,9 @@ def _decode_inputs(g, seqused, sq, hq, hkv, topk, npg_extra=3):
     for b, n in enumerate(pages):
         pt[b, :n] = perm[off:off + n]
         off += n
-    k = torch.randn(npg, hkv, 128, 128, generator=g).to(torch.bfloat16)
-    v = torch.randn(npg, hkv, 128, 128, generator=g).to(torch.bfloat16)
-    q = torch.randn(len(seqused) * sq, hq, 128, generator=g).to(torch.bfloat16)
+    k = torch.randn(npg, hkv, 128, 128, generator=g).to(dtype)
+    v = torch.randn(npg, hkv, 128, 128, generator=g).to(dtype)
+    q = torch.randn(len(seqused) * sq, hq, 128, generator=g).to(dtype)
     q2k = workloads.select_blocks(workloads.query_positions(cu_q, seqused), hkv, topk, g)
     return dict(q=q, k=k, v=v, q2k_indices=q2k, cu_seqlens_q=cu_q, page_table=pt,
                 seqused_k=torch.tensor(seqused, dtype=torch.int32))
@@ -327,6 +332,17 @@ def test_decode_graph_replay(msa):
         fault_clear(msa)
         ref_out, ref_lse = _oracle(new)
         check_attention(out, lse, ref_out, ref_lse, label=f"graph_replay_{trial}")
+
+
+@pytest.mark.parametrize("sq", [1, 4])
+def test_decode_f16(msa, sq):
+    seqused = [4000, 700, 129]
+    inp = _decode_inputs(torch.Generator().manual_seed(40 + sq), seqused, sq, 32, 2, 16,
+                         dtype=torch.float16)
+    out, lse = _run_prefill(msa, inp, max_seqlen_q=sq)
+    assert out.dtype == torch.float16
+    ref_out, ref_lse = _oracle(inp)
+    check_attention(out, lse, ref_out, ref_lse, label=f"f16_decode_sq{sq}")
 
 
 def test_decode_deterministic(msa):
