@@ -510,6 +510,52 @@ def bench_two_stage(msa, device, flush, seed=0):
     return res
 
 
+# ---------------------------------------------------------------- secondary: E4M3 K/V prefill
+def bench_e4m3(msa, device, flush, seed=0, reps=3):
+    """Flat varlen prefill with E4M3 K/V (upconverted in-kernel), bf16 q."""
+    spec = workloads.MIXED_E4M3
+    inp = workloads.make_prefill(spec, seed, device=device)
+    tq, hq, _ = inp["q"].shape
+    hkv = inp["k"].shape[1]
+    G = hq // hkv
+    max_sq = max(inp["lengths"])
+    cnt = visible_counts(inp["q2k_indices"], inp["cu_seqlens_q"], inp["lengths"])
+    flops = 4.0 * D * G * float(cnt.sum())
+    out = torch.empty_like(inp["q"])
+    lse = torch.empty((tq, hq), dtype=torch.float32, device=device)
+    need = msa.msa_sparse_attention_workspace_size(len(inp["lengths"]), tq, hq, hkv, D, spec.topk,
+                                                   max_sq, False)
+    ws = torch.empty(need, dtype=torch.uint8, device=device)
+    W = msa.msa_union_tile_tokens(hq, hkv)
+    ulen = msa.msa_build_union(inp["q2k_indices"], inp["cu_seqlens_q"], inp["cu_seqlens_k"],
+                               causal=True, tile_tokens=W)[0]
+    flops_exec = float(ulen.sum().item()) * 4.0 * D * 128 * 128
+    for _ in range(2):
+        run_prefill(msa, inp, out, lse, ws, max_sq)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    ts, ta = [], []
+    for _ in range(reps):
+        flush.fill_(1)
+        msa.msa_set_timing_events(ev)
+        run_prefill(msa, inp, out, lse, ws, max_sq)
+        ev[2].synchronize()
+        ts.append(ev[0].elapsed_time(ev[2]) * 1e-3)
+        ta.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+    msa.msa_set_timing_events(None)
+    t, t_attn = statistics.median(ts), statistics.median(ta)
+    pk = peaks()
+    res = {"workload": spec.name, "tokens": int(tq), "value": round(flops / t / 1e12, 2),
+           "unit": "TFLOP/s", "ms": round(t * 1e3, 3), "attention_ms": round(t_attn * 1e3, 3),
+           "roofline": {"bound": "tensor", "achieved": round(flops / t_attn / 1e12, 2),
+                        "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                        "frac": round(flops / t_attn / 1e12 / pk["bf16_sus"], 4)},
+           "executed_mma_tflops": round(flops_exec / t_attn / 1e12, 2),
+           "work_efficiency": round(flops / flops_exec, 4)}
+    del inp
+    torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------- reference arm: the oracle
 def reference_arm(args, world, rank):
     if rank != 0:
@@ -565,6 +611,8 @@ def main():
                     help="profiling case: prefill only, 1 x 8192 tokens, 64/8 heads, top-16")
     ap.add_argument("--profile-decode", type=int, default=0, metavar="SQ",
                     help="profiling case: paged decode only, 64 requests, seqlen_q SQ")
+    ap.add_argument("--profile-e4m3", action="store_true",
+                    help="profiling case: the E4M3 K/V varlen prefill only")
     ap.add_argument("--profile-two-stage", action="store_true",
                     help="profiling case: proxy score, top-k and attention of the two-stage "
                          "workload only")
@@ -587,6 +635,10 @@ def main():
                          reps=args.steps)
         print(json.dumps({"profile_decode": r}))
         return 0
+    if args.profile_e4m3:
+        flush = l2_flush_buffer(device)
+        print(json.dumps({"profile_e4m3": bench_e4m3(msa, device, flush, reps=args.steps)}))
+        return 0
     if args.profile_two_stage:
         flush = l2_flush_buffer(device)
         print(json.dumps({"profile_two_stage": bench_two_stage(msa, device, flush)}))
@@ -603,6 +655,8 @@ def main():
         secondary["decode"] = bench_decode(msa, device, flush)
         torch.cuda.empty_cache()
         secondary["two_stage"] = bench_two_stage(msa, device, flush)
+        torch.cuda.empty_cache()
+        secondary["e4m3_prefill"] = bench_e4m3(msa, device, flush)
     else:
         res.pop("inp")
     cpu = None

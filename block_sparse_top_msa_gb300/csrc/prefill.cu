@@ -79,10 +79,11 @@ struct Roles {
   static constexpr int kMmaWarp = kSoftmaxWarps + 1;
   static constexpr int kVProducerWarp = FP8 ? -1 : kSoftmaxWarps + 2;  // V (bf16 only)
   static constexpr int kConvWarp0 = kSoftmaxWarps + 2;              // E4M3 converters
-  static constexpr int kWarps = kSoftmaxWarps + (FP8 ? 6 : 3);
+  static constexpr int kConvWarps = 4;
+  static constexpr int kWarps = kSoftmaxWarps + 2 + (FP8 ? kConvWarps : 1);
   // Readers of the item ring (the K producer writes it): V producer (bf16),
   // the MMA issuer's two cursors, every softmax warp, every converter warp.
-  static constexpr int kItemReaders = (FP8 ? 0 : 1) + 2 + kSoftmaxWarps + (FP8 ? 4 : 0);
+  static constexpr int kItemReaders = (FP8 ? 0 : 1) + 2 + kSoftmaxWarps + (FP8 ? kConvWarps : 0);
   static constexpr int kThreads = kWarps * 32;
 };
 
@@ -194,28 +195,35 @@ MSA_DEV void exp_pack_store(const float* sv, float2 sc2, float neg_m, float2& ac
   if (N == 64) tmem_st32(pcol, pk);
 }
 
+// Four E4M3 ("fn") codes, lowest byte first, to four bf16 values (two packed
+// pairs), exactly: E4M3 -> f16 is exact, and so is f16 -> bf16 for every
+// E4M3 value (NaN stays NaN). (An integer-only decode that scales the placed
+// bits by 2^120 was measured slower than these conversions.)
+MSA_DEV void e4m3x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+#pragma unroll
+  for (int y = 0; y < 2; ++y) {
+    const uint16_t pair = (uint16_t)(w >> (16 * y));
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+    (y == 0 ? lo : hi) = pack_bf16x2(f.x, f.y);
+  }
+}
+
 // Upconverts one 128x128 E4M3 tile (TMA SWIZZLE_128B image, 128-byte rows)
-// into the two 64-column bf16 halves the MMA reads. 128 threads.
+// into the two 64-column bf16 halves the MMA reads, with kThreads threads.
+template <int kThreads>
 MSA_DEV void convert_tile(const uint8_t* src, uint8_t* dst_half0, int t) {
-#pragma unroll 2
-  for (int j = 0; j < 8; ++j) {
-    const int i = t + j * 128;
+#pragma unroll 4
+  for (int j = 0; j < 1024 / kThreads; ++j) {
+    const int i = t + j * kThreads;
     const int r = i >> 3, c = i & 7;
     const uint4 raw = *reinterpret_cast<const uint4*>(src + sw128_offset(r, c));
-    const uint32_t words[4] = {raw.x, raw.y, raw.z, raw.w};
     uint32_t outw[8];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-#pragma unroll
-      for (int y = 0; y < 2; ++y) {
-        const uint16_t pair = (uint16_t)(words[x] >> (16 * y));
-        uint32_t h2;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
-        const __half2 hh = *reinterpret_cast<const __half2*>(&h2);
-        const float2 f = __half22float2(hh);
-        outw[x * 2 + y] = pack_bf16x2(f.x, f.y);
-      }
-    }
+    e4m3x4_to_bf16(raw.x, outw[0], outw[1]);
+    e4m3x4_to_bf16(raw.y, outw[2], outw[3]);
+    e4m3x4_to_bf16(raw.z, outw[4], outw[5]);
+    e4m3x4_to_bf16(raw.w, outw[6], outw[7]);
     uint8_t* dst = dst_half0 + (c >> 2) * kTile;
     const int c16 = (c & 3) * 2;
     *reinterpret_cast<uint4*>(dst + sw128_offset(r, c16)) =
@@ -224,7 +232,6 @@ MSA_DEV void convert_tile(const uint8_t* src, uint8_t* dst_half0, int t) {
         make_uint4(outw[4], outw[5], outw[6], outw[7]);
   }
 }
-
 
 // The (t0, b) pair of item i's tile, the one field that needs a load before
 // the rest can be fetched (and that the softmax warps fetch one item ahead).
@@ -366,14 +373,14 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       mbar_init(&sm.q_empty[s], 1);
     }
     for (int s = 0; s < kKStages; ++s) {
-      mbar_init(&sm.k_full[s], FP8 ? 4 : 1);
+      mbar_init(&sm.k_full[s], FP8 ? R::kConvWarps : 1);
     }
     for (int s = 0; s < kVStages; ++s) {
-      mbar_init(&sm.v_full[s], FP8 ? 4 : 1);
+      mbar_init(&sm.v_full[s], FP8 ? R::kConvWarps : 1);
     }
     for (int s = 0; s < kF8Stages; ++s) {
       mbar_init(&sm.f8_full[s], 1);
-      mbar_init(&sm.f8_empty[s], 4);
+      mbar_init(&sm.f8_empty[s], R::kConvWarps);
     }
     for (int s = 0; s < kSBuf; ++s) {
       mbar_init(&sm.qk_done[s], 1);
@@ -639,7 +646,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       mma_commit(&sm.drain);
       mbar_wait(&sm.drain, 0, fault, kFaultWaitMma);
     }
-  } else if (FP8 && warp >= R::kConvWarp0 && warp < R::kConvWarp0 + 4) {
+  } else if (FP8 && warp >= R::kConvWarp0 && warp < R::kConvWarp0 + R::kConvWarps) {
     // ------------------------------------------------------------ E4M3 -> bf16
     const int ct = tid - R::kConvWarp0 * 32;
     int g = 0;
@@ -658,7 +665,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
           ok = false;
           break;
         }
-        convert_tile(sm.k8[s8], sm.k[ks][0], ct);
+        convert_tile<R::kConvWarps * 32>(sm.k8[s8], sm.k[ks][0], ct);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.k_full[ks]);
@@ -666,7 +673,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
           ok = false;
           break;
         }
-        convert_tile(sm.v8[s8], sm.v[vs][0], ct);
+        convert_tile<R::kConvWarps * 32>(sm.v8[s8], sm.v[vs][0], ct);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {

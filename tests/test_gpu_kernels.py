@@ -159,6 +159,29 @@ def test_prefill_parity(msa, case):
     check_attention(out, lse, ref_out, ref_lse, label=name)
 
 
+def test_prefill_e4m3_every_code(msa):
+    """K takes every non-NaN E4M3 code (zeros, subnormals, the largest
+    magnitudes) and V every code below 2 in magnitude, scattered at random,
+    so the in-kernel upconversion is checked code by code through the
+    attention result."""
+    inp = _prefill_inputs([300, 200], [300, 200], 8, 2, 4, seed=11, kv="e4m3")
+    g = torch.Generator().manual_seed(3)
+    k_codes = torch.tensor([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=torch.uint8)
+    v_codes = torch.tensor([c for c in range(256) if (c & 0x78) <= 0x38], dtype=torch.uint8)
+
+    def fill(codes, like):
+        n = like.numel()
+        rep = codes.repeat((n + codes.numel() - 1) // codes.numel())[:n]
+        return rep[torch.randperm(n, generator=g)].view(like.shape).view(torch.float8_e4m3fn)
+
+    inp["k"] = fill(k_codes, inp["k"])
+    inp["v"] = fill(v_codes, inp["v"])
+    inp["q"] = (inp["q"].float() / 64).to(torch.bfloat16)  # keeps logits moderate
+    out, lse = _run_prefill(msa, inp)
+    ref_out, ref_lse = _oracle(inp)
+    check_attention(out, lse, ref_out, ref_lse, label="e4m3_every_code")
+
+
 def test_prefill_non_causal_and_scale(msa):
     inp = _prefill_inputs([200, 300], [200, 300], 8, 2, 4, seed=9)
     out, lse = _run_prefill(msa, inp, causal=False, scale=0.05)
