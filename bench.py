@@ -444,10 +444,36 @@ def bench_decode(msa, device, flush, seed=0, small=False, sqs=(1, 4), reps=7):
             "roofline": {"bound": "hbm", "achieved": round(gbs_attn, 1), "peak": pk["hbm"],
                          "unit": "GB/s", "frac": round(gbs_attn / pk["hbm"], 4), "traffic": None,
                          "kernel": "prefill_kernel<bf16> (paged, split items)"}}
+        if sq == 1:
+            out["proxy_seqlen_q_1"] = bench_decode_proxy(msa, inp, flush, pk, reps)
         del inp
         torch.cuda.empty_cache()
     out["workload"] = spec.name
     return out
+
+
+def bench_decode_proxy(msa, inp, flush, pk, reps):
+    """Paged proxy scores (reduce_heads) of the decode batch: every key of every
+    request is visible to its one query token, so the kernel streams the whole
+    K cache; HBM-bound."""
+    q, k, pt, su = inp["q"], inp["k"], inp["page_table"], inp["seqused_k"]
+    T = pt.shape[1]
+    scores = torch.empty((1, T, q.shape[0]), dtype=torch.float32, device=q.device)
+
+    def call():
+        msa.msa_proxy_score(q, k, inp["cu_seqlens_q"], None, causal=True, max_k_tiles=T,
+                            reduce_heads=True, output=scores, page_table=pt, seqused_k=su,
+                            max_seqlen_q=1)
+
+    call()
+    t = time_launch(call, q.device, reps=reps, flush=flush)
+    kbytes = float(su.long().sum()) * k.shape[1] * D * 2
+    nbytes = kbytes + q.numel() * 2 + scores.numel() * 4 + pt.numel() * 4
+    return {"value": round(nbytes / t / 1e9, 1), "unit": "GB/s", "us": round(t * 1e6, 2),
+            "k_bytes": int(kbytes),
+            "roofline": {"bound": "hbm", "achieved": round(nbytes / t / 1e9, 1), "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": round(nbytes / t / 1e9 / pk["hbm"], 4),
+                         "kernel": "proxy_kernel (paged, column slices)"}}
 
 
 # ---------------------------------------------------------------- secondary: two-stage

@@ -183,29 +183,39 @@ def msa_sparse_attention_fwd(q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k=No
     return (out, lse) if lse is not None else out
 
 
-def msa_proxy_score(q, k, cu_seqlens_q, cu_seqlens_k, *, causal=True, max_k_tiles=None,
-                    reduce_heads=False, output=None, max_seqlen_q=None, stream=None):
-    """Per-block max of unscaled causal q.k; see ``msa_proxy_score`` in include/msa.h."""
+def msa_proxy_score(q, k, cu_seqlens_q, cu_seqlens_k=None, *, causal=True, max_k_tiles=None,
+                    reduce_heads=False, output=None, max_seqlen_q=None, page_table=None,
+                    seqused_k=None, stream=None):
+    """Per-block max of unscaled causal q.k; see ``msa_proxy_score`` in include/msa.h.
+
+    Flat K (Tk, Hkv, 128) with cu_seqlens_k, or a paged pool
+    (num_pages, Hkv, 128, 128) with page_table and seqused_k.
+    """
     L = lib()
     _cuda_contig("q", q)
     _cuda_contig("k", k)
     _cuda_contig("cu_seqlens_q", cu_seqlens_q, torch.int32)
     _cuda_contig("cu_seqlens_k", cu_seqlens_k, torch.int32)
+    _cuda_contig("page_table", page_table, torch.int32)
+    _cuda_contig("seqused_k", seqused_k, torch.int32)
     total_q, hq, d = q.shape
     hkv = k.shape[1]
     batch = cu_seqlens_q.shape[0] - 1
     if max_k_tiles is None:
-        max_k_tiles = max(1, (_max_len(cu_seqlens_k) + 127) // 128)
+        longest = (int(seqused_k.max().item()) if page_table is not None
+                   else _max_len(cu_seqlens_k))
+        max_k_tiles = max(1, (longest + 127) // 128)
     if max_seqlen_q is None:
         max_seqlen_q = 0
     if output is None:
         output = torch.empty(((1 if reduce_heads else hq), max_k_tiles, total_q),
                              dtype=torch.float32, device=q.device)
     _cuda_contig("output", output, torch.float32)
+    max_pages = page_table.shape[1] if page_table is not None else 0
     st = L.msa_proxy_score(_p(q), _dtype_code(q), _p(k), _dtype_code(k), _p(cu_seqlens_q),
-                           _p(cu_seqlens_k), None, 0, None, batch, total_q, k.shape[0], hq, hkv, d,
-                           int(max_seqlen_q), int(max_k_tiles), int(bool(causal)),
-                           int(bool(reduce_heads)), _p(output), _stream(stream))
+                           _p(cu_seqlens_k), _p(page_table), max_pages, _p(seqused_k), batch,
+                           total_q, k.shape[0], hq, hkv, d, int(max_seqlen_q), int(max_k_tiles),
+                           int(bool(causal)), int(bool(reduce_heads)), _p(output), _stream(stream))
     _check("msa_proxy_score", st)
     return output
 

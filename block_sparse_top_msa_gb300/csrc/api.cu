@@ -45,6 +45,9 @@ int tile_tokens_for(int hq, int hkv) {
 // (device-independent, so the workspace size query needs no device).
 constexpr int kPlanSMs = 152;
 constexpr int kMinSplitBlocks = 4;
+constexpr int kProxyFewTiles = 2;    // proxy tiles per SM below which columns are split
+constexpr int kProxyCtasPerSM = 16;  // proxy CTAs per SM aimed at when tiles are few
+constexpr int kProxyMinSlice = 16;   // fewest block columns per proxy CTA
 
 struct PrefillLayout {
   int W, max_tiles, cap, words;
@@ -317,20 +320,20 @@ msa_status_t msa_proxy_score(const void* q, msa_dtype_t q_dtype, const void* k,
                              int num_qo_heads, int num_kv_heads, int head_dim, int max_seqlen_q,
                              int max_k_tiles, int causal, int reduce_heads, float* output,
                              cudaStream_t stream) {
-  (void)max_pages;
-  (void)max_seqlen_q;
-  if (page_table != nullptr || seqused_k != nullptr) {
-    if (cu_seqlens_k != nullptr) return MSA_INVALID_ARG;
-    return MSA_UNSUPPORTED;  // the paged proxy is not built
-  }
-  if (q == nullptr || k == nullptr || cu_seqlens_q == nullptr || cu_seqlens_k == nullptr ||
-      output == nullptr)
+  const bool paged = page_table != nullptr;
+  const int num_pages = paged ? total_k : 0;  // paged: total_k counts the pool's pages
+  if (cu_seqlens_k != nullptr && paged) return MSA_INVALID_ARG;   // two length sources
+  if (cu_seqlens_k == nullptr && !paged) return MSA_INVALID_ARG;  // no length source
+  if (paged && (seqused_k == nullptr || max_pages < 1 || num_pages < 1)) return MSA_INVALID_ARG;
+  if (!paged && seqused_k != nullptr) return MSA_INVALID_ARG;
+  if (q == nullptr || k == nullptr || cu_seqlens_q == nullptr || output == nullptr)
     return MSA_INVALID_ARG;
-  if (batch < 1 || total_q < 0 || total_k < 1 || num_qo_heads < 1 || num_kv_heads < 1 ||
-      num_qo_heads % num_kv_heads != 0 || max_k_tiles < 1)
+  if (batch < 1 || total_q < 0 || total_k < 1 || num_qo_heads < 1 ||
+      num_kv_heads < 1 || num_qo_heads % num_kv_heads != 0 || max_k_tiles < 1)
     return MSA_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(output, 4) || !aligned(cu_seqlens_q, 4) ||
-      !aligned(cu_seqlens_k, 4))
+      (cu_seqlens_k && !aligned(cu_seqlens_k, 4)) || (page_table && !aligned(page_table, 4)) ||
+      (seqused_k && !aligned(seqused_k, 4)))
     return MSA_INVALID_ARG;
   if (head_dim != 128 || q_dtype != MSA_BF16 || k_dtype != MSA_BF16) return MSA_UNSUPPORTED;
   const int G = num_qo_heads / num_kv_heads;
@@ -341,11 +344,17 @@ msa_status_t msa_proxy_score(const void* q, msa_dtype_t q_dtype, const void* k,
   a.fault = fault_word();
   if (a.fault == nullptr) return MSA_CUDA_ERROR;
   const int Wm = tile_tokens_for(num_qo_heads, num_kv_heads);
-  if (!map_rows(&a.tmap_q, q, 2, num_qo_heads, total_q, (uint32_t)G, (uint32_t)Wm) ||
-      !map_rows(&a.tmap_k, k, 2, num_kv_heads, total_k, 1, 128))
-    return MSA_CUDA_ERROR;
+  bool ok = map_rows(&a.tmap_q, q, 2, num_qo_heads, total_q, (uint32_t)G, (uint32_t)Wm);
+  ok = ok && (paged ? map_pages(&a.tmap_k, k, 2, num_kv_heads, num_pages)
+                    : map_rows(&a.tmap_k, k, 2, num_kv_heads, total_k, 1, 128));
+  if (!ok) return MSA_CUDA_ERROR;
   a.cu_q = cu_seqlens_q;
   a.cu_k = cu_seqlens_k;
+  a.paged = paged ? 1 : 0;
+  a.page_table = page_table;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.seqused_k = seqused_k;
   a.batch = batch;
   a.total_q = total_q;
   a.num_qo_heads = num_qo_heads;
@@ -354,7 +363,26 @@ msa_status_t msa_proxy_score(const void* q, msa_dtype_t q_dtype, const void* k,
   a.causal = causal ? 1 : 0;
   a.reduce_heads = reduce_heads ? 1 : 0;
   a.tile_tokens = Wm;
-  a.max_tiles = (total_q + 2 * Wm - 1) / (2 * Wm) + batch;
+  // Query tiles of one M tile when max_seqlen_q (a bound on every Lq) says no
+  // sequence has more than Wm query tokens, else of two.
+  a.one_m = (max_seqlen_q > 0 && max_seqlen_q <= Wm) ? 1 : 0;
+  const int TQ = (a.one_m ? 1 : 2) * Wm;
+  a.max_tiles = (total_q + TQ - 1) / TQ + batch;
+  // Few tiles (decode-sized problems, under kProxyFewTiles per SM): split
+  // each tile's block columns into slices so that there are about
+  // kProxyCtasPerSM CTAs per SM, at least kProxyMinSlice columns each and at
+  // most what one pass over the groups holds (16384 / TQ columns).
+  const long long cap_cols = 16384 / TQ;
+  long long sc = max_k_tiles;
+  const long long target = (long long)kProxyCtasPerSM * kPlanSMs;
+  if ((long long)a.max_tiles < (long long)kProxyFewTiles * kPlanSMs) {
+    sc = ((long long)max_k_tiles * a.max_tiles + target - 1) / target;
+    if (sc < kProxyMinSlice) sc = kProxyMinSlice;
+  }
+  if (sc > cap_cols) sc = cap_cols;
+  if (sc > max_k_tiles) sc = max_k_tiles;
+  a.slice_cols = (int)sc;
+  a.slices = (int)((max_k_tiles + sc - 1) / sc);
   a.out = output;
   return from_cuda(launch_proxy(a, stream));
 }

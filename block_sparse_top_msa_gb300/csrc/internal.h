@@ -130,9 +130,14 @@ int device_sm_count();
 struct ProxyArgs {
   unsigned* fault;      // device fault word (bounded-wait expiry, capacity)
   CUtensorMap tmap_q;   // (d, Hq, Tq) bf16, box (64, G, Wm)
-  CUtensorMap tmap_k;   // (d, Hkv, Tk) bf16, box (64, 1, 128)
+  CUtensorMap tmap_k;   // flat (d, Hkv, Tk) / paged (d, 128, Hkv, pages) bf16, 128-key box
   const int32_t* cu_q;
-  const int32_t* cu_k;
+  const int32_t* cu_k;        // flat lengths, or NULL when paged
+  int paged;
+  const int32_t* page_table;  // (B, max_pages), paged only
+  int max_pages;
+  int num_pages;
+  const int32_t* seqused_k;   // (B), paged only
   int batch;
   int total_q;
   int num_qo_heads;
@@ -142,6 +147,9 @@ struct ProxyArgs {
   int reduce_heads;
   int tile_tokens;      // tokens per M-tile (128 / G)
   int max_tiles;        // upper bound on query tiles of 2 M-tiles each
+  int one_m;            // query tiles of tile_tokens tokens (one M tile), else 2 * tile_tokens
+  int slice_cols;       // block columns per CTA: CTA (tile, s) takes [s, s + 1) * slice_cols
+  int slices;           // column slices per tile
   float* out;
 };
 cudaError_t launch_proxy(const ProxyArgs& a, cudaStream_t s);

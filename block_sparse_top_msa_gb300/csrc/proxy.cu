@@ -4,9 +4,13 @@
 // above the causal limit give -inf; reduce_heads takes the max over query
 // heads as well).
 //
-// One CTA per query tile of 2 * Wm tokens (Wm = 128 / G), i.e. two tcgen05
-// M=128 tiles of (token, head-in-group) rows. Loop order: KV group g outer,
-// KV block t inner. For each (g, t) the producer warp TMA-loads K of block t
+// One CTA per (query tile of 2 * Wm tokens, slice of its block columns),
+// Wm = 128 / G: two tcgen05 M=128 tiles of (token, head-in-group) rows (the
+// second skipped when the tile has at most Wm tokens). A block column's max
+// needs no other slice, so decode-sized problems (few tokens, long contexts)
+// spread each tile's columns over many CTAs. K is flat or paged (one page
+// per block; an unmapped page gives -inf). Loop order: KV group g outer, KV
+// block t inner. For each (g, t) the producer warp TMA-loads K of block t
 // (128 x 128 bf16) into a two-stage ring; the MMA warp computes both tiles'
 // S = Q_g K_t^T into TMEM (double-buffered, 4 x 128 columns); eight epilogue
 // warps (two per TMEM lane quadrant, one per M tile) take each row's masked
@@ -45,7 +49,11 @@ struct __align__(1024) ProxySmem {
   int abort;
 };
 
+// PAGED: K from a page pool. ONE_M: query tiles of Wm tokens, one M tile
+// (decode-sized calls, where no sequence has more than Wm query tokens).
+template <bool PAGED, bool ONE_M>
 __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_constant__ ProxyArgs a) {
+  constexpr int MT = ONE_M ? 1 : 2;  // M tiles computed
   extern __shared__ uint8_t smem_raw[];
   ProxySmem& sm = *reinterpret_cast<ProxySmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -54,18 +62,20 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.num_qo_heads / a.num_kv_heads;
   const int Wm = a.tile_tokens;  // tokens per M tile
-  const int TQ = 2 * Wm;
-  const int tile = a.max_tiles - 1 - (int)blockIdx.x;
+  const int TQ = MT * Wm;        // tokens per query tile
+  const int tile = a.max_tiles - 1 - (int)(blockIdx.x / a.slices);
+  const int slice = (int)(blockIdx.x % a.slices);
 
   int b = 0, t0 = 0;
   if (!locate_tile(a.cu_q, a.batch, TQ, tile, sm.scan, &b, &t0)) return;
   const int seq_q0 = a.cu_q[b];
   const int lq = a.cu_q[b + 1] - seq_q0;
-  const int lk = a.cu_k[b + 1] - a.cu_k[b];
-  const int kv0 = a.cu_k[b];
+  const int lk = PAGED ? a.seqused_k[b] : a.cu_k[b + 1] - a.cu_k[b];
+  const int kv0 = PAGED ? 0 : a.cu_k[b];
   const int ntok = min(TQ, seq_q0 + lq - t0);
   int nblk = (lk + kBlk - 1) / kBlk;
   if (nblk > a.max_k_tiles) nblk = a.max_k_tiles;
+  if (PAGED && nblk > a.max_pages) nblk = a.max_pages;
   // Last block any token of the tile can see.
   int t_hi = nblk - 1;
   if (a.causal) {
@@ -73,9 +83,13 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
     const long long lim = pmax < 0 ? -1 : pmax / kBlk;
     if (lim < t_hi) t_hi = (int)lim;
   }
-  const int ncols = t_hi + 1;  // block columns computed; the rest are -inf
+  const int ncols = t_hi + 1;  // block columns with visible keys; the rest are -inf
+  // This CTA's columns [c_lo, c_lo + ncs); slice 0 also writes the -inf rest.
+  const int c_lo = min(ncols, slice * a.slice_cols);
+  const int ncs = min(ncols, c_lo + a.slice_cols) - c_lo;
+  if (ncs == 0 && slice > 0) return;
   const int CH = kPxRed / TQ;  // block columns per pass over the groups
-  const int nchunks = (ncols + CH - 1) / CH;
+  const int nchunks = (ncs + CH - 1) / CH;
   const int nsteps = nchunks * a.num_kv_heads;  // (chunk, group) passes
 
   if (tid == 0) {
@@ -101,11 +115,11 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
-  // Columns in chunk c: [c * CH, min(ncols, (c + 1) * CH)).
-  auto chunk_cols = [&](int c) { return min(CH, ncols - c * CH); };
+  // Columns in chunk c: c_lo + [c * CH, min(ncs, (c + 1) * CH)).
+  auto chunk_cols = [&](int c) { return min(CH, ncs - c * CH); };
 
   if (warp == kPxProducerWarp) {
-    if (lane == 0 && ncols > 0) {
+    if (lane == 0 && ncs > 0) {
       tma_prefetch_desc(&a.tmap_q);
       tma_prefetch_desc(&a.tmap_k);
       int it = 0;  // global K-tile counter
@@ -117,8 +131,8 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
           ok = false;
           break;
         }
-        mbar_expect_tx(&sm.q_full, 2u * 2u * 128u * (uint32_t)(G * Wm));
-        for (int m = 0; m < 2; ++m)
+        mbar_expect_tx(&sm.q_full, (uint32_t)MT * 2u * 128u * (uint32_t)(G * Wm));
+        for (int m = 0; m < MT; ++m)
           for (int hh = 0; hh < 2; ++hh)
             tma_load_3d(sm.q[m][hh], &a.tmap_q, &sm.q_full, hh * 64, g * G, t0 + m * Wm);
         const int nc = chunk_cols(c);
@@ -130,10 +144,18 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
             ok = false;
             break;
           }
-          const int t = c * CH + j;
+          const int t = c_lo + c * CH + j;
           mbar_expect_tx(&sm.k_full[st], 2 * kPxTile);
-          for (int hh = 0; hh < 2; ++hh)
-            tma_load_3d(sm.k[st][hh], &a.tmap_k, &sm.k_full[st], hh * 64, g, kv0 + t * kBlk);
+          if (PAGED) {
+            int page = a.page_table[(size_t)b * a.max_pages + t];
+            // An unmapped page reads as zeros (out-of-range box); the epilogue gives it -inf.
+            if (page < 0 || page >= a.num_pages) page = a.num_pages;
+            for (int hh = 0; hh < 2; ++hh)
+              tma_load_4d(sm.k[st][hh], &a.tmap_k, &sm.k_full[st], hh * 64, 0, g, page);
+          } else {
+            for (int hh = 0; hh < 2; ++hh)
+              tma_load_3d(sm.k[st][hh], &a.tmap_k, &sm.k_full[st], hh * 64, g, kv0 + t * kBlk);
+          }
           last_k[st] = it;
         }
       }
@@ -143,7 +165,7 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
       }
     }
   } else if (warp == kPxMmaWarp) {
-    if (lane == 0 && ncols > 0) {
+    if (lane == 0 && ncs > 0) {
       const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
       int it = 0;
       bool ok = true;
@@ -163,7 +185,8 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
             break;
           }
           tc_fence_after();
-          for (int m = 0; m < 2; ++m) {
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
             const uint32_t dcol = (uint32_t)(bb * 256 + m * 128);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -199,20 +222,27 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
       const int nc = chunk_cols(c);
       for (int j = 0; j < nc; ++j, ++it) {
         const int bb = it & 1;
-        const int t = c * CH + j;
+        const int t = c_lo + c * CH + j;
         ok = mbar_wait(&sm.s_full[bb], (it >> 1) & 1, fault, kFaultWaitMma, abort);
         if (__any_sync(0xffffffffu, !ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
+        // (With ONE_M, tile 1's columns are read unwritten and ignored: none
+        // of its rows is active.)
         float s[128];
         tmem_ld128(taddr_lane + (uint32_t)(bb * 256 + m * 128), s);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.s_free[bb]);
         float mx = -INFINITY;
-        if (active) {
+        bool page_ok = true;
+        if (PAGED) {
+          const int pg = __ldg(a.page_table + (size_t)b * a.max_pages + t);
+          page_ok = pg >= 0 && pg < a.num_pages;
+        }
+        if (active && page_ok) {
           long long last = (long long)lk - 1;
           if (a.causal && pos < last) last = pos;
           last -= (long long)t * kBlk;
@@ -241,9 +271,9 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
         }
       }
     }
-    // Columns no token of the tile can see.
+    // Columns no token of the tile can see (written by the tile's slice 0).
     const int heads_out = a.reduce_heads ? 1 : a.num_qo_heads;
-    const int rest = a.max_k_tiles - ncols;
+    const int rest = slice == 0 ? a.max_k_tiles - ncols : 0;
     for (long long i = tid; i < (long long)heads_out * rest * ntok; i += kPxEpiWarps * 32) {
       const int tt = (int)(i % ntok);
       const long long q2 = i / ntok;
@@ -264,10 +294,20 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
 
 cudaError_t launch_proxy(const ProxyArgs& a, cudaStream_t s) {
   const size_t smem = sizeof(ProxySmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(proxy_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = cudaSuccess;
+  for (auto k : {proxy_kernel<false, false>, proxy_kernel<false, true>, proxy_kernel<true, false>,
+                 proxy_kernel<true, true>})
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
   if (e != cudaSuccess) return e;
-  proxy_kernel<<<a.max_tiles, kPxThreads, smem, s>>>(a);
+  const dim3 grid((unsigned)((long long)a.max_tiles * a.slices));
+  if (a.paged) {
+    if (a.one_m) proxy_kernel<true, true><<<grid, kPxThreads, smem, s>>>(a);
+    else proxy_kernel<true, false><<<grid, kPxThreads, smem, s>>>(a);
+  } else {
+    if (a.one_m) proxy_kernel<false, true><<<grid, kPxThreads, smem, s>>>(a);
+    else proxy_kernel<false, false><<<grid, kPxThreads, smem, s>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -116,12 +116,26 @@ msa_status_t msa_sparse_attention_fwd(
  * has one head.
  *
  *   q            device, (Tq, Hq, 128), MSA_BF16
- *   k            device, flat (Tk, Hkv, 128), MSA_BF16
- *   cu_seqlens_q, cu_seqlens_k  device int32 (B+1)
- *   page_table, seqused_k       must be NULL (the paged proxy is not built)
+ *   k            device, MSA_BF16; flat (Tk, Hkv, 128) when page_table is
+ *                NULL, else a paged pool (num_pages, Hkv, 128, 128)
+ *   cu_seqlens_q device int32 (B+1)
+ *   cu_seqlens_k device int32 (B+1) for flat K; must be NULL when paged
+ *   page_table   device int32 (B, max_pages) mapping batch-local block ->
+ *                page, or NULL for flat K; requires seqused_k. A block whose
+ *                entry is negative or >= num_pages holds no key (-inf).
+ *   seqused_k    device int32 (B), keys per sequence (paged only)
+ *   total_k      keys in flat K, or num_pages, the pool's page count, when paged
+ *   max_seqlen_q host bound on every Lq, or 0 when unknown; a bound <= 128/G
+ *                lets query tiles hold one M=128 tile instead of two
  *   max_k_tiles  number of block columns; blocks >= ceil(Lk/128) read -inf
  *   output       device float32 (reduce_heads ? 1 : Hq, max_k_tiles, Tq),
  *                query fastest; fully written
+ * Decode-sized calls (few query tiles over long contexts) split each tile's
+ * block columns across many CTAs; a block's max needs no merge.
+ * Returns MSA_INVALID_ARG when both or neither of cu_seqlens_k and
+ * page_table are given, when a paged call lacks seqused_k or max_pages, or as
+ * for msa_sparse_attention_fwd; MSA_UNSUPPORTED for head_dim != 128, non-bf16
+ * operands, or reduce_heads with G = Hq / Hkv not a power of two <= 32.
  */
 msa_status_t msa_proxy_score(const void* q, msa_dtype_t q_dtype, const void* k,
                              msa_dtype_t k_dtype, const int32_t* cu_seqlens_q,

@@ -117,9 +117,14 @@ def test_forward_argument_errors(L):
 
 def test_other_entry_point_errors(L):
     vp = C.c_void_p
-    # proxy: paged form is not built; both length kinds -> invalid
+    # proxy: paged with head_dim 64 -> unsupported; paged without seqused_k or
+    # max_pages -> invalid; both length kinds -> invalid
     assert L.msa_proxy_score(vp(A), 0, vp(A), 0, vp(A), None, vp(A), 4, vp(A), 1, 128, 128, 8, 2,
-                             128, 128, 1, 1, 1, vp(A), None) == 2
+                             64, 128, 1, 1, 1, vp(A), None) == 2
+    assert L.msa_proxy_score(vp(A), 0, vp(A), 0, vp(A), None, vp(A), 4, None, 1, 128, 128, 8, 2,
+                             128, 128, 1, 1, 1, vp(A), None) == 1
+    assert L.msa_proxy_score(vp(A), 0, vp(A), 0, vp(A), None, vp(A), 0, vp(A), 1, 128, 128, 8, 2,
+                             128, 128, 1, 1, 1, vp(A), None) == 1
     assert L.msa_proxy_score(vp(A), 0, vp(A), 0, vp(A), vp(A), vp(A), 4, vp(A), 1, 128, 128, 8, 2,
                              128, 128, 1, 1, 1, vp(A), None) == 1
     assert L.msa_proxy_score(vp(A), 0, vp(A), 0, vp(A), vp(A), None, 0, None, 1, 128, 128, 8, 2,

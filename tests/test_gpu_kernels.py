@@ -385,6 +385,56 @@ def test_decode_deterministic(msa):
 
 
 # ---------------------------------------------------------------- proxy score
+PAGED_PROXY_CASES = [
+    # name, seqused, query tokens per request (None: as many as keys), hq, hkv, reduce,
+    # pass max_seqlen_q (decode: one M tile per query tile)
+    ("decode_sq1_reduce_g16", [8192, 300, 129, 128, 3000], 1, 32, 2, True, True),
+    ("decode_sq4_perhead_g8", [5000, 700], 4, 16, 2, False, True),
+    ("decode_sq1_reduce_long", [40000, 20000], 1, 64, 4, True, True),
+    ("decode_sq2_reduce_two_m_tiles", [3000, 900, 128], 2, 32, 2, True, False),
+    ("paged_prefill_reduce_g8", [300, 517], None, 16, 2, True, False),
+]
+
+
+@pytest.mark.parametrize("case", PAGED_PROXY_CASES, ids=[c[0] for c in PAGED_PROXY_CASES])
+def test_proxy_paged_parity(msa, case):
+    """Paged K (one page per block, a page table, seqused_k), including an
+    unmapped page; decode-sized cases run with their block columns split over
+    many CTAs."""
+    name, seqused, sq, hq, hkv, red, pass_sq = case
+    g = torch.Generator().manual_seed(len(name) + 300)
+    lens_q = list(seqused) if sq is None else [sq] * len(seqused)
+    cu_q = workloads.cu_from_lengths(lens_q)
+    pages = [(n + 127) // 128 for n in seqused]
+    npg = sum(pages) + 2
+    perm = torch.randperm(npg, generator=g).to(torch.int32)
+    pt = torch.zeros(len(seqused), max(pages), dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(pages):
+        pt[b, :n] = perm[off:off + n]
+        off += n
+    pt[1, 0] = npg + 5  # an unmapped page: its block holds no key
+    k = torch.randn(npg, hkv, 128, 128, generator=g).to(torch.bfloat16)
+    q = torch.randn(sum(lens_q), hq, 128, generator=g).to(torch.bfloat16)
+    su = torch.tensor(seqused, dtype=torch.int32)
+    T = max(pages) + 1
+    got = msa.msa_proxy_score(q.to(DEV), k.to(DEV), cu_q.to(DEV), None, causal=True,
+                              max_k_tiles=T, reduce_heads=red, page_table=pt.to(DEV),
+                              seqused_k=su.to(DEV), max_seqlen_q=max(lens_q) if pass_sq else None)
+    torch.cuda.synchronize()
+    fault_clear(msa)
+    rows = None
+    if q.shape[0] > 600:
+        rows = torch.tensor(sorted(set([0, 1, 127, 128, 129, q.shape[0] - 1] +
+                                       list(range(0, q.shape[0], 97)))), dtype=torch.int32)
+    ref = oracle.proxy_score(q, k, cu_q, None, page_table=pt, seqused_k=su, causal=True,
+                             max_k_tiles=T, reduce_heads=red, rows=rows)
+    gpu = got.cpu().numpy()
+    if rows is not None:
+        gpu = gpu[:, :, rows.long().numpy()]
+    check_proxy(gpu, ref, label=name)
+
+
 PROXY_CASES = [
     # name, lens_q, lens_k, hq, hkv, reduce, causal, extra_tiles
     ("reduce_g8", [300, 517], [300, 517], 16, 2, True, True, 0),

@@ -137,6 +137,25 @@ def test_paged_layout_equals_flat():
     np.testing.assert_array_equal(lse_p, lse_f)
 
 
+def test_paged_proxy_equals_flat():
+    """Paged addressing gives the flat proxy scores, per head and reduced."""
+    g = torch.Generator().manual_seed(6)
+    lens_k = [333, 700]
+    lens_q = [1, 300]
+    Hq, Hkv, d = 8, 2, 128
+    kf = torch.randn(sum(lens_k), Hkv, d, generator=g).to(torch.bfloat16)
+    q = torch.randn(sum(lens_q), Hq, d, generator=g).to(torch.bfloat16)
+    cu_q = workloads.cu_from_lengths(lens_q)
+    cu_k = workloads.cu_from_lengths(lens_k)
+    kp, pt = _to_paged(kf, lens_k, Hkv, d, torch.Generator().manual_seed(9))
+    su = torch.tensor(lens_k, dtype=torch.int32)
+    for red in (False, True):
+        flat = oracle.proxy_score(q, kf, cu_q, cu_k, causal=True, max_k_tiles=7, reduce_heads=red)
+        paged = oracle.proxy_score(q, kp, cu_q, None, page_table=pt, seqused_k=su, causal=True,
+                                   max_k_tiles=7, reduce_heads=red)
+        np.testing.assert_array_equal(paged, flat)
+
+
 def test_zero_query_closed_form():
     """q = 0: every visible logit is 0, so lse = ln|J| and out = mean of V over J.
 
