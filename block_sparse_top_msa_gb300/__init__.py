@@ -58,6 +58,14 @@ def lib():
         L.msa_sparse_attention_fwd.argtypes = [
             vp, i32, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, vp, i32, i32, i32, i32, i32,
             i32, i32, i32, f32, vp, vp, vp, sz, vp]
+        L.msa_sparse_attention_prepare.restype = i32
+        L.msa_sparse_attention_prepare.argtypes = [
+            vp, i32, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, vp, i32, i32, i32, i32, i32,
+            i32, i32, i32, f32, vp, vp, vp, sz, C.POINTER(vp)]
+        L.msa_sparse_attention_run.restype = i32
+        L.msa_sparse_attention_run.argtypes = [vp, vp]
+        L.msa_sparse_attention_plan_free.restype = None
+        L.msa_sparse_attention_plan_free.argtypes = [vp]
         L.msa_proxy_score.restype = i32
         L.msa_proxy_score.argtypes = [
             vp, i32, vp, i32, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
@@ -149,6 +157,18 @@ def msa_sparse_attention_fwd(q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k=No
     Returns ``out`` or ``(out, lse)``.
     """
     L = lib()
+    args, out, lse, workspace = _forward_args(
+        q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k, causal, softmax_scale, page_table,
+        seqused_k, max_seqlen_q, return_softmax_lse, out, lse, workspace)
+    st = L.msa_sparse_attention_fwd(*args, _stream(stream))
+    _check("msa_sparse_attention_fwd", st)
+    return (out, lse) if lse is not None else out
+
+
+def _forward_args(q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k, causal, softmax_scale,
+                  page_table, seqused_k, max_seqlen_q, return_softmax_lse, out, lse, workspace):
+    """The C arguments of a forward (all but the stream), allocating out, lse
+    and workspace when not given."""
     _cuda_contig("q", q)
     _cuda_contig("k", k)
     _cuda_contig("v", v)
@@ -172,15 +192,49 @@ def msa_sparse_attention_fwd(q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k=No
                                                max(1, max_seqlen_q), paged)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
-    st = L.msa_sparse_attention_fwd(
-        _p(q), _dtype_code(q), _p(k), _p(v), _dtype_code(k), _p(q2k_indices), topk,
-        _p(cu_seqlens_q), _p(cu_seqlens_k), _p(page_table),
-        page_table.shape[1] if paged else 0, k.shape[0] if paged else 0, _p(seqused_k), batch,
-        total_q, 0 if paged else k.shape[0], hq, hkv, d, int(max_seqlen_q), int(bool(causal)),
-        float(softmax_scale) if softmax_scale is not None else 0.0, _p(out), _p(lse),
-        _p(workspace), workspace.numel(), _stream(stream))
-    _check("msa_sparse_attention_fwd", st)
-    return (out, lse) if lse is not None else out
+    args = (_p(q), _dtype_code(q), _p(k), _p(v), _dtype_code(k), _p(q2k_indices), topk,
+            _p(cu_seqlens_q), _p(cu_seqlens_k), _p(page_table),
+            page_table.shape[1] if paged else 0, k.shape[0] if paged else 0, _p(seqused_k),
+            batch, total_q, 0 if paged else k.shape[0], hq, hkv, d, int(max_seqlen_q),
+            int(bool(causal)), float(softmax_scale) if softmax_scale is not None else 0.0,
+            _p(out), _p(lse), _p(workspace), workspace.numel())
+    return args, out, lse, workspace
+
+
+class SparseAttentionRunner:
+    """A forward prepared once (``msa_sparse_attention_prepare``) and launched
+    by ``run()`` (``msa_sparse_attention_run``): no allocation, no host
+    synchronisation and no argument processing per launch; capturable into a
+    CUDA graph. The tensors given here are bound by address: refill them in
+    place between runs. ``out`` and ``lse`` hold the results."""
+
+    def __init__(self, q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k=None, *, causal=False,
+                 softmax_scale=None, page_table=None, seqused_k=None, max_seqlen_q=None,
+                 return_softmax_lse=False, out=None, lse=None, workspace=None):
+        L = lib()
+        args, self.out, self.lse, self.workspace = _forward_args(
+            q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k, causal, softmax_scale, page_table,
+            seqused_k, max_seqlen_q, return_softmax_lse, out, lse, workspace)
+        # Keep every bound buffer alive as long as the plan.
+        self._bound = (q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k, page_table, seqused_k)
+        plan = C.c_void_p()
+        _check("msa_sparse_attention_prepare",
+               L.msa_sparse_attention_prepare(*args, C.byref(plan)))
+        self._plan = plan
+        self._lib = L
+
+    def run(self, stream=None):
+        _check("msa_sparse_attention_run",
+               self._lib.msa_sparse_attention_run(self._plan, _stream(stream)))
+        return (self.out, self.lse) if self.lse is not None else self.out
+
+    def close(self):
+        if getattr(self, "_plan", None):
+            self._lib.msa_sparse_attention_plan_free(self._plan)
+            self._plan = None
+
+    def __del__(self):
+        self.close()
 
 
 def msa_proxy_score(q, k, cu_seqlens_q, cu_seqlens_k=None, *, causal=True, max_k_tiles=None,

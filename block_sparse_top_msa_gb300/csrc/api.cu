@@ -6,6 +6,9 @@
 #include <string.h>
 
 #include <mutex>
+#include <new>
+#include <tuple>
+#include <vector>
 
 #include "../../include/msa.h"
 #include "internal.h"
@@ -159,6 +162,40 @@ void mark(int i, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t set_smem_limit(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::vector<std::tuple<const void*, int, int>> done;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (const auto& t : done)
+      if (std::get<0>(t) == kernel && std::get<1>(t) == dev && std::get<2>(t) >= bytes)
+        return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) {
+    std::lock_guard<std::mutex> lk(mu);
+    done.emplace_back(kernel, dev, bytes);
+  }
+  return e;
+}
+
+int device_smem_optin() {
+  static int cache[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 0;
+  if (cache[dev] == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return 0;
+    cache[dev] = v;
+  }
+  return cache[dev];
+}
+
 }  // namespace msa
 
 using namespace msa;
@@ -191,13 +228,25 @@ size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_he
   return prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q).total;
 }
 
-msa_status_t msa_sparse_attention_fwd(
+}  // extern "C"
+
+namespace msa {
+namespace {
+
+// Everything a forward launch needs, decided and encoded on the host.
+struct ForwardPlan {
+  bool empty = true;  // total_q == 0: nothing to launch
+  UnionArgs u{};
+  PrefillArgs a{};
+};
+
+msa_status_t build_forward(
     const void* q, msa_dtype_t q_dtype, const void* k, const void* v, msa_dtype_t kv_dtype,
     const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
     const int32_t* cu_seqlens_k, const int32_t* page_table, int max_pages, int num_pages,
     const int32_t* seqused_k, int batch, int total_q, int total_k, int num_qo_heads,
     int num_kv_heads, int head_dim, int max_seqlen_q, int causal, float softmax_scale, void* out,
-    float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    float* lse, void* workspace, size_t workspace_bytes, ForwardPlan* plan) {
   // ---- argument checks (host only; nothing is read from the device) ----
   const bool paged = page_table != nullptr;
   if (cu_seqlens_k != nullptr && paged) return MSA_INVALID_ARG;   // two length sources
@@ -228,7 +277,8 @@ msa_status_t msa_sparse_attention_fwd(
   const size_t need = msa_sparse_attention_workspace_size(
       batch, total_q, num_qo_heads, num_kv_heads, head_dim, topk, max_seqlen_q, paged ? 1 : 0);
   if (workspace_bytes < need || (need > 0 && workspace == nullptr)) return MSA_WORKSPACE_TOO_SMALL;
-  if (total_q == 0) return MSA_OK;
+  plan->empty = total_q == 0;
+  if (plan->empty) return MSA_OK;
   unsigned* fault = fault_word();
   if (fault == nullptr) return MSA_CUDA_ERROR;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
@@ -238,7 +288,7 @@ msa_status_t msa_sparse_attention_fwd(
 
   const PrefillLayout L =
       prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q);
-  UnionArgs u{};
+  UnionArgs& u = plan->u;
   u.q2k = q2k_indices;
   u.topk = topk;
   u.cu_q = cu_seqlens_q;
@@ -258,12 +308,7 @@ msa_status_t msa_sparse_attention_fwd(
   u.member = reinterpret_cast<uint32_t*>(ws + L.off_member);
   u.tile_info = reinterpret_cast<int32_t*>(ws + L.off_info);
   u.item_counter = reinterpret_cast<int32_t*>(ws + L.off_counter);
-  mark(0, stream);
-  cudaError_t e = launch_build_union(u, stream);
-  if (e != cudaSuccess) return MSA_CUDA_ERROR;
-  mark(1, stream);
-
-  PrefillArgs a{};
+  PrefillArgs& a = plan->a;
   a.fault = fault;
   bool ok = map_rows(&a.tmap_q, q, 2, num_qo_heads, total_q, (uint32_t)G, (uint32_t)L.W);
   if (paged) {
@@ -308,10 +353,77 @@ msa_status_t msa_sparse_attention_fwd(
   a.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
   a.part_ml = reinterpret_cast<float*>(ws + L.off_part_ml);
   a.item_counter = u.item_counter;
-  e = launch_prefill(a, stream);
+  return MSA_OK;
+}
+
+msa_status_t launch_forward(const ForwardPlan& p, cudaStream_t stream) {
+  if (p.empty) return MSA_OK;
+  mark(0, stream);
+  cudaError_t e = launch_build_union(p.u, stream);
+  if (e != cudaSuccess) return MSA_CUDA_ERROR;
+  mark(1, stream);
+  e = launch_prefill(p.a, stream);
   mark(2, stream);
   return from_cuda(e);
 }
+
+}  // namespace
+}  // namespace msa
+
+struct msa_attention_plan {
+  msa::ForwardPlan p;
+};
+
+extern "C" {
+
+#define MSA_FWD_ARGS                                                                           \
+  q, q_dtype, k, v, kv_dtype, q2k_indices, topk, cu_seqlens_q, cu_seqlens_k, page_table,    \
+      max_pages, num_pages, seqused_k, batch, total_q, total_k, num_qo_heads, num_kv_heads, \
+      head_dim, max_seqlen_q, causal, softmax_scale, out, lse, workspace, workspace_bytes
+
+msa_status_t msa_sparse_attention_fwd(
+    const void* q, msa_dtype_t q_dtype, const void* k, const void* v, msa_dtype_t kv_dtype,
+    const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, const int32_t* page_table, int max_pages, int num_pages,
+    const int32_t* seqused_k, int batch, int total_q, int total_k, int num_qo_heads,
+    int num_kv_heads, int head_dim, int max_seqlen_q, int causal, float softmax_scale, void* out,
+    float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  msa::ForwardPlan p;
+  const msa_status_t st = msa::build_forward(MSA_FWD_ARGS, &p);
+  if (st != MSA_OK) return st;
+  return msa::launch_forward(p, stream);
+}
+
+msa_status_t msa_sparse_attention_prepare(
+    const void* q, msa_dtype_t q_dtype, const void* k, const void* v, msa_dtype_t kv_dtype,
+    const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, const int32_t* page_table, int max_pages, int num_pages,
+    const int32_t* seqused_k, int batch, int total_q, int total_k, int num_qo_heads,
+    int num_kv_heads, int head_dim, int max_seqlen_q, int causal, float softmax_scale, void* out,
+    float* lse, void* workspace, size_t workspace_bytes, msa_attention_plan_t** plan_out) {
+  if (plan_out == nullptr) return MSA_INVALID_ARG;
+  *plan_out = nullptr;
+  msa_attention_plan_t* plan = new (std::nothrow) msa_attention_plan_t;
+  if (plan == nullptr) return MSA_CUDA_ERROR;
+  const msa_status_t st = msa::build_forward(MSA_FWD_ARGS, &plan->p);
+  if (st != MSA_OK) {
+    delete plan;
+    return st;
+  }
+  *plan_out = plan;
+  return MSA_OK;
+}
+
+msa_status_t msa_sparse_attention_run(const msa_attention_plan_t* plan, cudaStream_t stream) {
+  if (plan == nullptr) return MSA_INVALID_ARG;
+  return msa::launch_forward(plan->p, stream);
+}
+
+void msa_sparse_attention_plan_free(msa_attention_plan_t* plan) { delete plan; }
+
+#undef MSA_FWD_ARGS
+
+
 
 msa_status_t msa_proxy_score(const void* q, msa_dtype_t q_dtype, const void* k,
                              msa_dtype_t k_dtype, const int32_t* cu_seqlens_q,

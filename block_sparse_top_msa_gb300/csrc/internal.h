@@ -126,6 +126,11 @@ struct PrefillArgs {
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 int device_sm_count();
+// Raises `kernel`'s dynamic shared-memory limit to at least `bytes` on the
+// current device; the driver call is made once per (kernel, device, size).
+cudaError_t set_smem_limit(const void* kernel, int bytes);
+// The current device's per-block shared-memory limit (opt-in), cached.
+int device_smem_optin();
 
 struct ProxyArgs {
   unsigned* fault;      // device fault word (bounded-wait expiry, capacity)

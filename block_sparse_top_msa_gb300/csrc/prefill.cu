@@ -1015,15 +1015,11 @@ template <bool FP8, bool STREAM, bool F16>
 cudaError_t launch_t(const PrefillArgs& a, cudaStream_t s) {
   // Up to 1 KiB of slack for aligning the base, within the per-block limit
   // (the kernel checks that the slack it got covers its base's offset).
-  int optin = 0, dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess)
-    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if (e != cudaSuccess) return e;
+  const int optin = device_smem_optin();
+  if (optin <= 0) return cudaErrorInvalidDevice;
   size_t smem = sizeof(PrefillSmem<FP8, STREAM>) + 1024;
   if (smem > (size_t)optin) smem = (size_t)optin;
-  e = cudaFuncSetAttribute(prefill_kernel<FP8, STREAM, F16>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_limit((const void*)prefill_kernel<FP8, STREAM, F16>, (int)smem);
   if (e != cudaSuccess) return e;
   const int grid = a.num_items < device_sm_count() ? a.num_items : device_sm_count();
   if (grid <= 0) return cudaSuccess;

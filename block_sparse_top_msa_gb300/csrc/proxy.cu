@@ -297,8 +297,7 @@ cudaError_t launch_proxy(const ProxyArgs& a, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   for (auto k : {proxy_kernel<false, false>, proxy_kernel<false, true>, proxy_kernel<true, false>,
                  proxy_kernel<true, true>})
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)smem);
+    if (e == cudaSuccess) e = set_smem_limit((const void*)k, (int)smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((long long)a.max_tiles * a.slices));
   if (a.paged) {

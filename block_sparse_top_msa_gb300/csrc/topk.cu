@@ -326,8 +326,7 @@ cudaError_t launch_k(const TopkArgs& a, cudaStream_t s) {
 template <int K>
 cudaError_t launch_buffered(const TopkArgs& a, cudaStream_t s) {
   dim3 grid((a.total_q + kTopkThreads - 1) / kTopkThreads, a.num_score_heads);
-  cudaError_t e = cudaFuncSetAttribute(topk_buffered_kernel<K>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBufferedSmem);
+  cudaError_t e = set_smem_limit((const void*)topk_buffered_kernel<K>, (int)kBufferedSmem);
   if (e != cudaSuccess) return e;
   topk_buffered_kernel<K><<<grid, kTopkThreads, kBufferedSmem, s>>>(a.scores, a.num_score_heads, a.max_k_tiles,
                                                          a.total_q, a.topk, a.num_kv_heads_out, a.q2k);

@@ -256,8 +256,7 @@ cudaError_t launch_build_union(const UnionArgs& a, cudaStream_t s) {
     const int nt = P < 32 ? 32 : P;
     const size_t smem =
         sizeof(int) * ((size_t)nt + 2 + a.cap + (size_t)a.tile_tokens * a.words);
-    cudaError_t e = cudaFuncSetAttribute(build_union_small_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_smem_limit((const void*)build_union_small_kernel, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.max_tiles, a.num_kv_heads);
     build_union_small_kernel<<<grid, nt, smem, s>>>(a);
@@ -266,8 +265,7 @@ cudaError_t launch_build_union(const UnionArgs& a, cudaStream_t s) {
   const size_t smem =
       sizeof(int) * ((size_t)kUnionThreads + 2 + P + a.cap + (size_t)a.tile_tokens * a.words);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(build_union_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = set_smem_limit((const void*)build_union_kernel, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.max_tiles, a.num_kv_heads);
   build_union_kernel<<<grid, kUnionThreads, smem, s>>>(a);

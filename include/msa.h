@@ -106,6 +106,32 @@ msa_status_t msa_sparse_attention_fwd(
     float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Prepared forward: msa_sparse_attention_prepare takes exactly the arguments
+ * of msa_sparse_attention_fwd (without the stream), checks them with the same
+ * rules and statuses, and binds them: the work split, the workspace layout
+ * and the TMA descriptors are decided once, on the host, with no device
+ * access. msa_sparse_attention_run then launches that forward on `stream`
+ * with no allocation, no host synchronisation and no argument processing;
+ * it can be captured into a CUDA graph. The bound device buffers must stay
+ * allocated while the plan is used; their contents may change between runs
+ * (each run reads them afresh). A plan is host memory owned by the caller,
+ * released with msa_sparse_attention_plan_free (NULL is accepted). (The
+ * prepare / runner split follows the interface the pages give for
+ * "prepare_msa_nvfp4_sparse_decode"; here it serves the bf16, fp16 and E4M3
+ * routes of msa_sparse_attention_fwd.)
+ */
+typedef struct msa_attention_plan msa_attention_plan_t;
+msa_status_t msa_sparse_attention_prepare(
+    const void* q, msa_dtype_t q_dtype, const void* k, const void* v, msa_dtype_t kv_dtype,
+    const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, const int32_t* page_table, int max_pages, int num_pages,
+    const int32_t* seqused_k, int batch, int total_q, int total_k, int num_qo_heads,
+    int num_kv_heads, int head_dim, int max_seqlen_q, int causal, float softmax_scale, void* out,
+    float* lse, void* workspace, size_t workspace_bytes, msa_attention_plan_t** plan);
+msa_status_t msa_sparse_attention_run(const msa_attention_plan_t* plan, cudaStream_t stream);
+void msa_sparse_attention_plan_free(msa_attention_plan_t* plan);
+
+/*
  * Dense proxy pass, MSA stage 1 ("flashinfer.msa_ops.msa_proxy_score").
  *
  * output[h, t, q] = max over the keys j of KV block t of the UNSCALED logit

@@ -115,6 +115,42 @@ def test_forward_argument_errors(L):
     assert fwd(L, total_q=0) == 0                    # nothing to do, no launch
 
 
+def test_prepared_forward_host_paths(L):
+    """prepare applies the forward's checks (and leaves no plan on failure);
+    an empty problem gives a plan whose run launches nothing."""
+    vp = C.c_void_p
+
+    def prepare(**kw):
+        args = dict(q=A, qdt=0, k=A, v=A, kvdt=0, q2k=A, topk=16, cu_q=A, cu_k=A, pt=None,
+                    max_pages=0, num_pages=0, su=None, batch=1, total_q=128, total_k=128, hq=8,
+                    hkv=2, d=128, max_sq=128, causal=1, scale=0.0, out=A, lse=None, ws=A,
+                    ws_bytes=1 << 40)
+        args.update(kw)
+        p = vp(123)
+        v_ = lambda x: None if x is None else vp(x)
+        st = L.msa_sparse_attention_prepare(
+            v_(args["q"]), args["qdt"], v_(args["k"]), v_(args["v"]), args["kvdt"],
+            v_(args["q2k"]), args["topk"], v_(args["cu_q"]), v_(args["cu_k"]), v_(args["pt"]),
+            args["max_pages"], args["num_pages"], v_(args["su"]), args["batch"], args["total_q"],
+            args["total_k"], args["hq"], args["hkv"], args["d"], args["max_sq"], args["causal"],
+            args["scale"], v_(args["out"]), v_(args["lse"]), v_(args["ws"]), args["ws_bytes"],
+            C.byref(p))
+        return st, p
+
+    st, p = prepare(hq=8, hkv=3)
+    assert st == 1 and not p.value
+    st, p = prepare(d=64)
+    assert st == 2 and not p.value
+    st, p = prepare(ws_bytes=16)
+    assert st == 3 and not p.value
+    st, p = prepare(total_q=0)
+    assert st == 0 and p.value
+    assert L.msa_sparse_attention_run(p, None) == 0  # nothing to launch
+    L.msa_sparse_attention_plan_free(p)
+    assert L.msa_sparse_attention_run(None, None) == 1
+    L.msa_sparse_attention_plan_free(None)
+
+
 def test_other_entry_point_errors(L):
     vp = C.c_void_p
     # proxy: paged with head_dim 64 -> unsupported; paged without seqused_k or

@@ -368,6 +368,40 @@ def test_decode_f16(msa, sq):
     check_attention(out, lse, ref_out, ref_lse, label=f"f16_decode_sq{sq}")
 
 
+def test_prepared_runner_matches_forward(msa):
+    """A prepared forward gives the plain forward's bits, refilled inputs give
+    fresh results, and its run captures into a CUDA graph."""
+    seqused, sq, hq, hkv, topk = [2500, 900, 129], 4, 32, 2, 16
+    host = _decode_inputs(torch.Generator().manual_seed(21), seqused, sq, hq, hkv, topk)
+    dev = to_dev(host, DEV)
+    kw = dict(causal=True, page_table=dev["page_table"], seqused_k=dev["seqused_k"],
+              max_seqlen_q=sq, return_softmax_lse=True)
+    ref_o, ref_l = msa.msa_sparse_attention_fwd(dev["q"], dev["k"], dev["v"], dev["q2k_indices"],
+                                                dev["cu_seqlens_q"], None, **kw)
+    runner = msa.SparseAttentionRunner(dev["q"], dev["k"], dev["v"], dev["q2k_indices"],
+                                       dev["cu_seqlens_q"], None, **kw)
+    o, l = runner.run()
+    torch.cuda.synchronize()
+    fault_clear(msa)
+    assert torch.equal(o, ref_o) and torch.equal(l, ref_l)
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            runner.run()
+    new = _decode_inputs(torch.Generator().manual_seed(22), seqused, sq, hq, hkv, topk)
+    for key in ("q", "k", "v", "q2k_indices"):
+        dev[key].copy_(new[key])
+    graph.replay()
+    torch.cuda.synchronize()
+    fault_clear(msa)
+    new["page_table"], new["seqused_k"] = host["page_table"], host["seqused_k"]
+    ref_out, ref_lse = _oracle(new)
+    check_attention(runner.out, runner.lse, ref_out, ref_lse, label="runner_graph")
+    runner.close()
+
+
 def test_decode_deterministic(msa):
     g = torch.Generator().manual_seed(0)
     seqused = [3000, 900]
