@@ -46,36 +46,6 @@ struct TopkArgs {
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t s);
 
-struct DecodeArgs {
-  unsigned* fault;      // device fault word (bounded-wait expiry, capacity)
-  CUtensorMap tmap_q;   // (d, Hq, Tq) bf16, box (64, G, sq_max)
-  CUtensorMap tmap_k;   // (d, 128, Hkv, pages) bf16, box (64, 128, 1, 1)
-  CUtensorMap tmap_v;
-  const int32_t* q2k;
-  int topk;
-  const int32_t* cu_q;
-  const int32_t* page_table;
-  int max_pages;
-  int num_pages;
-  const int32_t* seqused_k;
-  int batch;
-  int total_q;
-  int num_qo_heads;
-  int num_kv_heads;
-  int sq_max;           // max_seqlen_q (<= 4)
-  int causal;
-  float scale_log2;     // softmax_scale * log2(e)
-  void* out;
-  float* lse;
-  int pages_per_split;
-  int splits;           // per (request, kv head)
-  float* part_o;        // (B*Hkv*splits, rows_max, 128)
-  float* part_ml;       // (B*Hkv*splits, rows_max, 2)
-  int* tickets;         // (B*Hkv)
-};
-cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
-size_t decode_workspace_bytes(int batch, int num_kv_heads, int rows_max, int splits);
-int decode_pages_per_split(int rows);
 
 struct PrefillArgs {
   unsigned* fault;      // device fault word (bounded-wait expiry, capacity)

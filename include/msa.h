@@ -246,24 +246,20 @@ msa_status_t msa_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t str
  * Engines that plan all device memory ahead of time, plugin interfaces that
  * give a kernel no workspace, and code running where cudaMalloc may not be
  * called cannot provide the workspace msa_sparse_attention_fwd needs. This
- * entry point computes the same result as msa_sparse_attention_fwd on its
- * split-KV decode route (paged bf16 K/V, max_seqlen_q <= 4, G <= 16,
- * head_dim 128, topk <= 64; arguments as there, q and K/V bf16) but keeps its
- * scratch in a fixed 16 MiB array inside the library's device image, which
- * every GPU that loads the library holds until the process exits. It
- * allocates nothing. The scratch it needs is
- *   align256(P * R * 512) + align256(P * R * 8) + align256(batch * Hkv * 4) bytes,
- * R = 16, 32 or 64 (s_q * G rounded up), P = batch * Hkv * ceil(s_q * topk / S),
- * S = 4 pages per split when s_q * G <= 16 and 8 otherwise; larger problems
- * are rejected with MSA_WORKSPACE_TOO_SMALL before anything is launched.
+ * entry point is msa_sparse_attention_fwd for a paged call with bf16 q and
+ * K/V (arguments as there; same kernels, same result bits), with the
+ * workspace taken from a fixed 16 MiB array inside the library's device
+ * image, which every GPU that loads the library holds until the process
+ * exits. It allocates nothing. Calls whose workspace
+ * (msa_sparse_attention_workspace_size with paged = 1) exceeds the array are
+ * rejected with MSA_WORKSPACE_TOO_SMALL before anything is launched;
  * msa_sparse_decode_noalloc_scratch_limit() returns the array size.
  *
  * The first call on a device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream
  * capture. All calls share the one array and it keeps the previous call's
- * contents: the completion tickets are cleared on `stream` before every
- * launch, and calls whose work overlaps on the GPU race on the array, so
- * callers must order them.
+ * contents (the forward needs no initialised workspace); calls whose work
+ * overlaps on the GPU race on the array, so callers must order them.
  */
 msa_status_t msa_sparse_decode_noalloc(
     const void* q, const void* k, const void* v, const int32_t* q2k_indices, int topk,
