@@ -369,7 +369,9 @@ def bench_prefill(msa, args, device, world, rank):
         e2e_step(i)
     torch.cuda.synchronize(device)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_e2e = max(3, min(args.steps, 10))
+    # At least 10 steps: the pipeline's fill (first copy-in) and drain (last
+    # copy-out) are paid once per timed run.
+    n_e2e = max(10, args.steps)
     s.record(s_in)
     for i in range(n_e2e):
         e2e_step(i)
