@@ -54,6 +54,8 @@ def lib():
         L.msa_status_string.argtypes = [i32]
         L.msa_sparse_attention_workspace_size.restype = sz
         L.msa_sparse_attention_workspace_size.argtypes = [i32] * 8
+        L.msa_sparse_attention_workspace_size_kv.restype = sz
+        L.msa_sparse_attention_workspace_size_kv.argtypes = [i32] * 10
         L.msa_sparse_attention_fwd.restype = i32
         L.msa_sparse_attention_fwd.argtypes = [
             vp, i32, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, vp, i32, i32, i32, i32, i32,
@@ -148,6 +150,15 @@ def msa_sparse_attention_workspace_size(batch, total_q, num_qo_heads, num_kv_hea
         batch, total_q, num_qo_heads, num_kv_heads, head_dim, topk, max_seqlen_q, int(bool(paged))))
 
 
+def msa_sparse_attention_workspace_size_kv(batch, total_q, num_qo_heads, num_kv_heads, head_dim,
+                                           topk, max_seqlen_q, paged, kv_dtype, total_k) -> int:
+    """``kv_dtype`` is a torch dtype or an MSA_* code."""
+    code = kv_dtype if isinstance(kv_dtype, int) else _dtype_code(torch.empty(0, dtype=kv_dtype))
+    return int(lib().msa_sparse_attention_workspace_size_kv(
+        batch, total_q, num_qo_heads, num_kv_heads, head_dim, topk, max_seqlen_q, int(bool(paged)),
+        code, total_k))
+
+
 def msa_sparse_attention_fwd(q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k=None, *,
                              causal=False, softmax_scale=None, page_table=None, seqused_k=None,
                              max_seqlen_q=None, return_softmax_lse=False, out=None, lse=None,
@@ -188,9 +199,10 @@ def _forward_args(q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k, causal, soft
         out = torch.empty_like(q)
     if lse is None and return_softmax_lse:
         lse = torch.empty((total_q, hq), dtype=torch.float32, device=q.device)
-    need = msa_sparse_attention_workspace_size(batch, total_q, hq, hkv, d, topk,
-                                               max(1, max_seqlen_q), paged)
     if workspace is None:
+        need = msa_sparse_attention_workspace_size_kv(batch, total_q, hq, hkv, d, topk,
+                                                      max(1, max_seqlen_q), paged, _dtype_code(k),
+                                                      0 if paged else k.shape[0])
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     args = (_p(q), _dtype_code(q), _p(k), _p(v), _dtype_code(k), _p(q2k_indices), topk,
             _p(cu_seqlens_q), _p(cu_seqlens_k), _p(page_table),

@@ -133,6 +133,23 @@ PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk, 
   return L;
 }
 
+// Flat E4M3 K/V on a prefill-sized call (at least as many query rows x query
+// heads as key rows x KV heads) is decoded to bf16 once, into the workspace,
+// and attended with the bf16 kernel: the attention kernel is tensor-bound
+// there, and converting in the kernel costs it more than the HBM-bound
+// decode pass does. Decode-sized calls (few query rows over long contexts)
+// read each selected block about once, so they keep the E4M3 bytes and
+// convert in the kernel.
+bool kv_decode_route(msa_dtype_t kv_dtype, bool paged, long long total_q, int hq,
+                     long long total_k, int hkv) {
+  return kv_dtype == MSA_FP8_E4M3 && !paged && total_k > 0 &&
+         total_q * hq >= total_k * hkv;
+}
+// Bytes of one bf16 copy of a flat (total_k, hkv, 128) tensor, 256-aligned.
+size_t kv_copy_bytes(long long total_k, int hkv) {
+  return up256((size_t)total_k * (size_t)hkv * 128 * 2);
+}
+
 // (d, H, T) map over a (T, H, d) tensor; element size 2 (bf16) or 1 (e4m3).
 bool map_rows(CUtensorMap* m, const void* base, int esize, int H, long long T, uint32_t box_h,
               uint32_t box_t) {
@@ -228,6 +245,18 @@ size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_he
   return prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q).total;
 }
 
+size_t msa_sparse_attention_workspace_size_kv(int batch, int total_q, int num_qo_heads,
+                                              int num_kv_heads, int head_dim, int topk,
+                                              int max_seqlen_q, int paged, msa_dtype_t kv_dtype,
+                                              int total_k) {
+  const size_t base = msa_sparse_attention_workspace_size(
+      batch, total_q, num_qo_heads, num_kv_heads, head_dim, topk, max_seqlen_q, paged);
+  if (base == 0 || total_k < 0) return 0;
+  if (!kv_decode_route(kv_dtype, paged != 0, total_q, num_qo_heads, total_k, num_kv_heads))
+    return base;
+  return base + 2 * kv_copy_bytes(total_k, num_kv_heads);
+}
+
 }  // extern "C"
 
 namespace msa {
@@ -236,6 +265,7 @@ namespace {
 // Everything a forward launch needs, decided and encoded on the host.
 struct ForwardPlan {
   bool empty = true;  // total_q == 0: nothing to launch
+  KvDecodeArgs dq{};  // n16 > 0: E4M3 K/V decoded to bf16 before the union kernel
   UnionArgs u{};
   PrefillArgs a{};
 };
@@ -283,8 +313,22 @@ msa_status_t build_forward(
   if (fault == nullptr) return MSA_CUDA_ERROR;
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
   const float scale_log2 = scale * 1.4426950408889634f;
-  const int esize = kv_dtype == MSA_FP8_E4M3 ? 1 : 2;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // The bf16-copy route needs its two copies after the layout's regions; with
+  // a smaller workspace the kernel converts E4M3 itself.
+  const size_t copy = kv_copy_bytes(total_k, num_kv_heads);
+  if (kv_decode_route(kv_dtype, paged, total_q, num_qo_heads, total_k, num_kv_heads) &&
+      workspace_bytes >= need + 2 * copy) {
+    plan->dq.k8 = k;
+    plan->dq.v8 = v;
+    plan->dq.k16 = ws + need;
+    plan->dq.v16 = ws + need + copy;
+    plan->dq.n16 = (size_t)total_k * num_kv_heads * 128 / 16;
+    k = plan->dq.k16;
+    v = plan->dq.v16;
+    kv_dtype = MSA_BF16;
+  }
+  const int esize = kv_dtype == MSA_FP8_E4M3 ? 1 : 2;
 
   const PrefillLayout L =
       prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q);
@@ -359,7 +403,9 @@ msa_status_t build_forward(
 msa_status_t launch_forward(const ForwardPlan& p, cudaStream_t stream) {
   if (p.empty) return MSA_OK;
   mark(0, stream);
-  cudaError_t e = launch_build_union(p.u, stream);
+  cudaError_t e = launch_kv_decode(p.dq, stream);
+  if (e != cudaSuccess) return MSA_CUDA_ERROR;
+  e = launch_build_union(p.u, stream);
   if (e != cudaSuccess) return MSA_CUDA_ERROR;
   mark(1, stream);
   e = launch_prefill(p.a, stream);

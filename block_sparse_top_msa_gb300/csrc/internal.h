@@ -129,4 +129,14 @@ struct ProxyArgs {
 };
 cudaError_t launch_proxy(const ProxyArgs& a, cudaStream_t s);
 
+// Flat E4M3 K and V (n16 16-byte groups each) decoded to bf16 copies.
+struct KvDecodeArgs {
+  const void* k8 = nullptr;
+  const void* v8 = nullptr;
+  void* k16 = nullptr;
+  void* v16 = nullptr;
+  size_t n16 = 0;
+};
+cudaError_t launch_kv_decode(const KvDecodeArgs& a, cudaStream_t s);
+
 }  // namespace msa

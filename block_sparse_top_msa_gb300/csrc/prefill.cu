@@ -195,21 +195,6 @@ MSA_DEV void exp_pack_store(const float* sv, float2 sc2, float neg_m, float2& ac
   if (N == 64) tmem_st32(pcol, pk);
 }
 
-// Four E4M3 ("fn") codes, lowest byte first, to four bf16 values (two packed
-// pairs), exactly: E4M3 -> f16 is exact, and so is f16 -> bf16 for every
-// E4M3 value (NaN stays NaN). (An integer-only decode that scales the placed
-// bits by 2^120 was measured slower than these conversions.)
-MSA_DEV void e4m3x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-#pragma unroll
-  for (int y = 0; y < 2; ++y) {
-    const uint16_t pair = (uint16_t)(w >> (16 * y));
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
-    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-    (y == 0 ? lo : hi) = pack_bf16x2(f.x, f.y);
-  }
-}
-
 // Upconverts one 128x128 E4M3 tile (TMA SWIZZLE_128B image, 128-byte rows)
 // into the two 64-column bf16 halves the MMA reads, with kThreads threads.
 template <int kThreads>

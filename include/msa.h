@@ -54,6 +54,22 @@ size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_he
                                            int max_seqlen_q, int paged);
 
 /*
+ * Workspace bytes for the forward's fastest route with these K/V: the size
+ * above, plus, for flat MSA_FP8_E4M3 K/V on a prefill-sized call (total_q *
+ * num_qo_heads >= total_k * num_kv_heads), room for a bf16 copy of K and of
+ * V (2 * 256-byte-rounded total_k * num_kv_heads * head_dim * 2 bytes). Given
+ * that much, the forward decodes E4M3 K/V into the copy with one HBM-bound
+ * pass and runs the attention kernel on bf16 operands; given only the size
+ * above, the attention kernel converts E4M3 itself (same results, slower on
+ * tensor-bound calls). Equals the size above for every other case; total_k
+ * is ignored when paged. Returns 0 where the size above does or total_k < 0.
+ */
+size_t msa_sparse_attention_workspace_size_kv(int batch, int total_q, int num_qo_heads,
+                                              int num_kv_heads, int head_dim, int topk,
+                                              int max_seqlen_q, int paged, msa_dtype_t kv_dtype,
+                                              int total_k);
+
+/*
  * Sparse attention forward ("flashinfer.msa_ops.msa_sparse_attention").
  *
  * Each query token t and query head h attends only to the keys of the 128-token
@@ -71,8 +87,10 @@ size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_he
  *   q            device, (Tq, Hq, d), q_dtype MSA_BF16 or MSA_FP16
  *   k, v         device; flat (Tk, Hkv, d) when page_table == NULL, else
  *                paged (num_pages, Hkv, BLK, d); kv_dtype: with bf16 q,
- *                MSA_BF16 or MSA_FP8_E4M3 (E4M3 "fn", upconverted exactly
- *                in-kernel); with fp16 q, MSA_FP16
+ *                MSA_BF16 or MSA_FP8_E4M3 (E4M3 "fn", decoded exactly to
+ *                bf16: by a pass into the workspace when it holds
+ *                msa_sparse_attention_workspace_size_kv(...) bytes, else in
+ *                the attention kernel); with fp16 q, MSA_FP16
  *   q2k_indices  device int32 (Hkv, Tq, topk); 1 <= topk <= 64
  *   cu_seqlens_q device int32 (B+1), cumulative query lengths
  *   cu_seqlens_k device int32 (B+1) for flat K/V; must be NULL when paged
@@ -88,9 +106,11 @@ size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_he
  *   out          device, (Tq, Hq, d), dtype of q; fully written
  *   lse          device float32 (Tq, Hq) or NULL
  *   workspace    device scratch of at least
- *                msa_sparse_attention_workspace_size(...) bytes, 256-byte
- *                aligned; its contents need no initialisation, and calls that
- *                share one workspace must be ordered on the device.
+ *                msa_sparse_attention_workspace_size(...) bytes (or the
+ *                larger msa_sparse_attention_workspace_size_kv(...), see
+ *                there), 256-byte aligned; its contents need no
+ *                initialisation, and calls that share one workspace must be
+ *                ordered on the device.
  * Returns MSA_INVALID_ARG when both or neither of cu_seqlens_k and page_table
  * are given (paged length comes only from seqused_k, per the page's rule of
  * declining two possibly disagreeing length sources), when Hq % Hkv != 0, or

@@ -7,6 +7,7 @@ import re
 import subprocess
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "msa.h")
@@ -71,6 +72,37 @@ def test_tile_tokens_and_workspace_size(L):
     paged = msa.msa_sparse_attention_workspace_size(128, 512, 64, 4, 128, 16, 4, 1)
     flat = msa.msa_sparse_attention_workspace_size(128, 512, 64, 4, 128, 16, 4, 0)
     assert paged >= flat > 0
+
+
+def test_workspace_size_with_kv_route(L):
+    """The K/V-aware size adds two 256-byte-rounded bf16 copies of K and V
+    exactly for flat E4M3 K/V on prefill-sized calls (query rows x query heads
+    at least key rows x KV heads), and equals the plain size otherwise."""
+    import block_sparse_top_msa_gb300 as msa
+    BF16, FP16, E4M3 = 0, 1, 2
+    args = (2, 65536, 32, 4, 128, 16, 32768)
+    base = msa.msa_sparse_attention_workspace_size(*args, 0)
+    copy = (65536 * 4 * 128 * 2 + 255) // 256 * 256
+    assert msa.msa_sparse_attention_workspace_size_kv(*args, 0, E4M3, 65536) == base + 2 * copy
+    assert msa.msa_sparse_attention_workspace_size_kv(*args, 0, BF16, 65536) == base
+    assert msa.msa_sparse_attention_workspace_size_kv(*args, 0, FP16, 65536) == base
+    # paged E4M3 and decode-sized flat E4M3 keep the in-kernel conversion
+    assert (msa.msa_sparse_attention_workspace_size_kv(*args, 1, E4M3, 65536)
+            == msa.msa_sparse_attention_workspace_size(*args, 1))
+    dec = (128, 128, 32, 4, 128, 16, 1)
+    assert (msa.msa_sparse_attention_workspace_size_kv(*dec, 0, E4M3, 128 * 8192)
+            == msa.msa_sparse_attention_workspace_size(*dec, 0))
+    # the boundary of the rule: total_q * Hq == total_k * Hkv takes the copy
+    edge = (1, 1000, 32, 4, 128, 16, 1000)
+    e_base = msa.msa_sparse_attention_workspace_size(*edge, 0)
+    assert msa.msa_sparse_attention_workspace_size_kv(*edge, 0, E4M3, 8000) == e_base + 2 * (
+        (8000 * 4 * 256 + 255) // 256 * 256)
+    assert msa.msa_sparse_attention_workspace_size_kv(*edge, 0, E4M3, 8001) == e_base
+    assert msa.msa_sparse_attention_workspace_size_kv(2, 100, 64, 8, 64, 16, 50, 0, E4M3, 100) == 0
+    assert msa.msa_sparse_attention_workspace_size_kv(*args, 0, E4M3, -1) == 0
+    # the torch-dtype spelling of the binding
+    assert (msa.msa_sparse_attention_workspace_size_kv(*args, 0, torch.float8_e4m3fn, 65536)
+            == base + 2 * copy)
 
 
 A = 0x10000  # a 64 KiB-aligned fake device address; never dereferenced on these paths

@@ -48,12 +48,13 @@ def _prefill_inputs(lens_q, lens_k, hq, hkv, topk, seed, kv="bf16", first_prev=F
     return dict(q=q, k=k, v=v, q2k_indices=q2k, cu_seqlens_q=cu_q, cu_seqlens_k=cu_k)
 
 
-def _run_prefill(msa, inp, causal=True, scale=None, max_seqlen_q=None):
+def _run_prefill(msa, inp, causal=True, scale=None, max_seqlen_q=None, workspace=None):
     g = to_dev(inp, DEV)
     out, lse = msa.msa_sparse_attention_fwd(
         g["q"], g["k"], g["v"], g["q2k_indices"], g["cu_seqlens_q"], g.get("cu_seqlens_k"),
         causal=causal, softmax_scale=scale, page_table=g.get("page_table"),
-        seqused_k=g.get("seqused_k"), max_seqlen_q=max_seqlen_q, return_softmax_lse=True)
+        seqused_k=g.get("seqused_k"), max_seqlen_q=max_seqlen_q, return_softmax_lse=True,
+        workspace=workspace)
     torch.cuda.synchronize()
     fault_clear(msa)
     return out, lse
@@ -159,11 +160,23 @@ def test_prefill_parity(msa, case):
     check_attention(out, lse, ref_out, ref_lse, label=name)
 
 
-def test_prefill_e4m3_every_code(msa):
+def _plain_workspace(msa, inp, hq, hkv, topk):
+    """A workspace of the plain size query: E4M3 K/V then convert in-kernel."""
+    lq = inp["cu_seqlens_q"]
+    n = msa.msa_sparse_attention_workspace_size(
+        lq.numel() - 1, inp["q"].shape[0], hq, hkv, 128, topk,
+        int((lq[1:] - lq[:-1]).max()), False)
+    return torch.empty(n, dtype=torch.uint8, device=DEV)
+
+
+@pytest.mark.parametrize("route", ["bf16_copy", "in_kernel"])
+def test_prefill_e4m3_every_code(msa, route):
     """K takes every non-NaN E4M3 code (zeros, subnormals, the largest
     magnitudes) and V every code below 2 in magnitude, scattered at random,
-    so the in-kernel upconversion is checked code by code through the
-    attention result."""
+    so the E4M3 -> bf16 decode is checked code by code through the attention
+    result, on both routes: the decode pass into the workspace's bf16 copy
+    (prefill-sized call, full workspace) and the conversion inside the
+    attention kernel (plain-size workspace)."""
     inp = _prefill_inputs([300, 200], [300, 200], 8, 2, 4, seed=11, kv="e4m3")
     g = torch.Generator().manual_seed(3)
     k_codes = torch.tensor([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=torch.uint8)
@@ -177,9 +190,37 @@ def test_prefill_e4m3_every_code(msa):
     inp["k"] = fill(k_codes, inp["k"])
     inp["v"] = fill(v_codes, inp["v"])
     inp["q"] = (inp["q"].float() / 64).to(torch.bfloat16)  # keeps logits moderate
-    out, lse = _run_prefill(msa, inp)
+    ws = _plain_workspace(msa, inp, 8, 2, 4) if route == "in_kernel" else None
+    out, lse = _run_prefill(msa, inp, workspace=ws)
     ref_out, ref_lse = _oracle(inp)
-    check_attention(out, lse, ref_out, ref_lse, label="e4m3_every_code")
+    check_attention(out, lse, ref_out, ref_lse, label=f"e4m3_every_code_{route}")
+
+
+def test_e4m3_bf16_copy_bit_exact(msa):
+    """The decode pass writes K and V as bf16 right after the layout's regions
+    of the workspace: bit-identical to torch's exact E4M3 -> bf16 cast for
+    every code, NaN codes included (compared as NaN)."""
+    lens = [700, 333]
+    inp = _prefill_inputs(lens, lens, 8, 2, 4, seed=21, kv="e4m3")
+    n = inp["k"].numel()
+    codes = torch.arange(n, dtype=torch.int64) % 256
+    inp["k"] = codes.to(torch.uint8).view(inp["k"].shape).view(torch.float8_e4m3fn)
+    inp["v"] = (255 - codes).to(torch.uint8).view(inp["v"].shape).view(torch.float8_e4m3fn)
+    inp["q"] = torch.zeros_like(inp["q"])
+    tq = inp["q"].shape[0]
+    base = msa.msa_sparse_attention_workspace_size(2, tq, 8, 2, 128, 4, max(lens), False)
+    full = msa.msa_sparse_attention_workspace_size_kv(2, tq, 8, 2, 128, 4, max(lens), False,
+                                                      torch.float8_e4m3fn, sum(lens))
+    copy = (n * 2 + 255) // 256 * 256
+    assert full == base + 2 * copy
+    ws = torch.zeros(full, dtype=torch.uint8, device=DEV)
+    _run_prefill(msa, inp, workspace=ws)
+    for name, off in (("k", base), ("v", base + copy)):
+        got = ws[off:off + 2 * n].view(torch.bfloat16).cpu().view(torch.int16)
+        want = inp[name].to(torch.bfloat16).view(torch.int16)
+        nan = torch.isnan(inp[name].to(torch.float32)).flatten()
+        assert torch.isnan(got.view(torch.bfloat16)[nan]).all(), name
+        assert torch.equal(got[~nan], want.flatten()[~nan]), name
 
 
 def test_prefill_non_causal_and_scale(msa):
