@@ -454,6 +454,68 @@ def bench_decode(msa, device, flush, seed=0, small=False, sqs=(1, 4), reps=7):
     return out
 
 
+def bench_decode_nvfp4(msa, device, flush, seed=0, sqs=(1, 4), reps=7):
+    """Paged decode with packed NVFP4 K/V (planar page pool, E4M3 block scales,
+    global scales): the same batch, selection and metric as the bf16 decode;
+    K/V bytes are 64 code + 8 scale bytes per token and side."""
+    spec = workloads.PAGED_DECODE_NVFP4
+    out = {}
+    pk = peaks()
+    for sq in sqs:
+        inp = workloads.make_decode(spec, seed, device=device, seqlen_q=sq)
+        q2k, pt, su = inp["q2k_indices"], inp["page_table"], inp["seqused_k"]
+        hkv = q2k.shape[0]
+        kk, ks, vv, vs = msa.nvfp4_views(inp["kv_pool"], hkv)
+        B = pt.shape[0]
+        ids = q2k.view(hkv, B, sq * q2k.shape[2]).long()
+        srt, _ = torch.sort(torch.where(ids >= 0, ids, torch.full_like(ids, 1 << 40)), dim=-1)
+        first = torch.ones_like(srt, dtype=torch.bool)
+        first[..., 1:] = srt[..., 1:] != srt[..., :-1]
+        valid = torch.clamp(torch.minimum(su.long()[None, :, None] - srt * 128,
+                                          torch.full_like(srt, 128)), min=0)
+        valid = torch.where((srt < (1 << 40)) & first, valid, torch.zeros_like(valid))
+        kv_bytes = float(valid.sum()) * (D // 2 + D // 16) * 2
+        meta = (inp["q"].numel() * 2 * 2 + inp["q"].shape[0] * inp["q"].shape[1] * 4 +
+                q2k.numel() * 4 + pt.numel() * 4)
+        o = torch.empty_like(inp["q"])
+        lse = torch.empty(inp["q"].shape[:2], dtype=torch.float32, device=device)
+        need = msa.msa_sparse_attention_workspace_size(B, inp["q"].shape[0], inp["q"].shape[1],
+                                                       hkv, D, q2k.shape[2], sq, True)
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+
+        def call():
+            msa.msa_sparse_attention_nvfp4_paged(
+                inp["q"], kk, ks, vv, vs, q2k, inp["cu_seqlens_q"], page_table=pt, seqused_k=su,
+                k_global_scale=inp["k_global_scale"], v_global_scale=inp["v_global_scale"],
+                max_seqlen_q=sq, out=o, lse=lse, workspace=ws)
+
+        for _ in range(3):
+            call()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ts, ta = [], []
+        for _ in range(reps):
+            flush.fill_(1)
+            msa.msa_set_timing_events(ev)
+            call()
+            ev[2].synchronize()
+            ts.append(ev[0].elapsed_time(ev[2]) * 1e-3)
+            ta.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+        msa.msa_set_timing_events(None)
+        t, t_attn = statistics.median(ts), statistics.median(ta)
+        gbs, gbs_attn = (kv_bytes + meta) / t / 1e9, (kv_bytes + meta) / t_attn / 1e9
+        out[f"seqlen_q_{sq}"] = {
+            "value": round(gbs, 1), "unit": "GB/s", "us": round(t * 1e6, 2),
+            "attention_us": round(t_attn * 1e6, 2), "kv_bytes": int(kv_bytes),
+            "meta_bytes": int(meta),
+            "roofline": {"bound": "hbm", "achieved": round(gbs_attn, 1), "peak": pk["hbm"],
+                         "unit": "GB/s", "frac": round(gbs_attn / pk["hbm"], 4), "traffic": None,
+                         "kernel": "prefill_kernel<E4M3 instance, NVFP4 staging> (paged)"}}
+        del inp
+        torch.cuda.empty_cache()
+    out["workload"] = spec.name
+    return out
+
+
 def bench_decode_proxy(msa, inp, flush, pk, reps):
     """Paged proxy scores (reduce_heads) of the decode batch: every key of every
     request is visible to its one query token, so the kernel streams the whole
@@ -653,6 +715,8 @@ def main():
                     help="profiling case: paged decode only, 64 requests, seqlen_q SQ")
     ap.add_argument("--profile-e4m3", action="store_true",
                     help="profiling case: the E4M3 K/V varlen prefill only")
+    ap.add_argument("--profile-nvfp4", action="store_true",
+                    help="profiling case: the packed NVFP4 paged decode only")
     ap.add_argument("--profile-two-stage", action="store_true",
                     help="profiling case: proxy score, top-k and attention of the two-stage "
                          "workload only")
@@ -675,6 +739,11 @@ def main():
                          reps=args.steps)
         print(json.dumps({"profile_decode": r}))
         return 0
+    if args.profile_nvfp4:
+        flush = l2_flush_buffer(device)
+        print(json.dumps({"profile_nvfp4": bench_decode_nvfp4(msa, device, flush,
+                                                              reps=args.steps)}))
+        return 0
     if args.profile_e4m3:
         flush = l2_flush_buffer(device)
         print(json.dumps({"profile_e4m3": bench_e4m3(msa, device, flush, reps=args.steps)}))
@@ -693,6 +762,8 @@ def main():
         del inp_keep
         torch.cuda.empty_cache()
         secondary["decode"] = bench_decode(msa, device, flush)
+        torch.cuda.empty_cache()
+        secondary["decode_nvfp4"] = bench_decode_nvfp4(msa, device, flush)
         torch.cuda.empty_cache()
         secondary["two_stage"] = bench_two_stage(msa, device, flush)
         torch.cuda.empty_cache()

@@ -68,6 +68,12 @@ def lib():
         L.msa_sparse_attention_run.argtypes = [vp, vp]
         L.msa_sparse_attention_plan_free.restype = None
         L.msa_sparse_attention_plan_free.argtypes = [vp]
+        fp4 = [vp, i32, vp, vp, vp, vp, C.c_longlong, f32, f32, vp, i32, vp, vp, i32, i32, vp, i32,
+               i32, i32, i32, i32, i32, f32, vp, vp, vp, sz]
+        L.msa_sparse_attention_nvfp4_paged.restype = i32
+        L.msa_sparse_attention_nvfp4_paged.argtypes = fp4 + [vp]
+        L.msa_sparse_attention_nvfp4_prepare.restype = i32
+        L.msa_sparse_attention_nvfp4_prepare.argtypes = fp4 + [C.POINTER(vp)]
         L.msa_proxy_score.restype = i32
         L.msa_proxy_score.argtypes = [
             vp, i32, vp, i32, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
@@ -247,6 +253,101 @@ class SparseAttentionRunner:
 
     def __del__(self):
         self.close()
+
+
+def nvfp4_views(kv_pool: torch.Tensor, num_kv_heads: int, head_dim: int = 128):
+    """(k, k_scale, v, v_scale) strided uint8 views of a planar NVFP4 page pool
+    (num_pages, page_stride) laid out [K data | K scales | V data | V scales]
+    per page: (num_pages, Hkv, 128, d/2) codes and (num_pages, Hkv, 128, d/16)
+    scales ("msa_sparse_attention": k, k_scale, v_scale)."""
+    npg, stride = kv_pool.shape
+    data, sc = num_kv_heads * 128 * head_dim // 2, num_kv_heads * 128 * head_dim // 16
+    flat = kv_pool.reshape(-1)
+
+    def view(off, inner):
+        return flat.as_strided((npg, num_kv_heads, 128, inner),
+                               (stride, 128 * inner, inner, 1), off)
+    return (view(0, head_dim // 2), view(data, head_dim // 16), view(data + sc, head_dim // 2),
+            view(2 * data + sc, head_dim // 16))
+
+
+def _fp4_args(q, k, k_scale, v, v_scale, q2k_indices, cu_seqlens_q, page_table, seqused_k,
+              k_global_scale, v_global_scale, max_seqlen_q, softmax_scale, return_softmax_lse,
+              out, lse, workspace):
+    _cuda_contig("q", q)
+    for name, t in (("q2k_indices", q2k_indices), ("cu_seqlens_q", cu_seqlens_q),
+                    ("page_table", page_table), ("seqused_k", seqused_k)):
+        _cuda_contig(name, t, torch.int32)
+    views = (k, k_scale, v, v_scale)
+    for name, t in zip(("k", "k_scale", "v", "v_scale"), views):
+        if not t.is_cuda or t.dtype not in (torch.uint8, torch.float8_e4m3fn) or t.dim() != 4:
+            raise ValueError(f"{name} must be a 4-d uint8 CUDA view of the page pool")
+        inner = t.shape[3]
+        if t.stride()[1:] != (128 * inner, inner, 1):
+            raise ValueError(f"{name}: (head, token, byte) must be contiguous within a page")
+    stride = k.stride(0)
+    if any(t.stride(0) != stride for t in views):
+        raise ValueError("k, k_scale, v and v_scale must share one page stride")
+    total_q, hq, d = q.shape
+    hkv, topk = k.shape[1], q2k_indices.shape[2]
+    batch = cu_seqlens_q.shape[0] - 1
+    if max_seqlen_q is None:
+        max_seqlen_q = _max_len(cu_seqlens_q)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_softmax_lse:
+        lse = torch.empty((total_q, hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = msa_sparse_attention_workspace_size(batch, total_q, hq, hkv, d, topk,
+                                                   max(1, max_seqlen_q), True)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    args = (_p(q), _dtype_code(q), _p(k), _p(k_scale), _p(v), _p(v_scale), stride,
+            float(k_global_scale), float(v_global_scale), _p(q2k_indices), topk, _p(cu_seqlens_q),
+            _p(page_table), page_table.shape[1], k.shape[0], _p(seqused_k), batch, total_q, hq,
+            hkv, d, int(max_seqlen_q),
+            float(softmax_scale) if softmax_scale is not None else 0.0, _p(out), _p(lse),
+            _p(workspace), workspace.numel())
+    return args, out, lse, workspace
+
+
+def msa_sparse_attention_nvfp4_paged(q, k, k_scale, v, v_scale, q2k_indices, cu_seqlens_q, *,
+                                     page_table, seqused_k, k_global_scale, v_global_scale,
+                                     max_seqlen_q=None, softmax_scale=None,
+                                     return_softmax_lse=False, out=None, lse=None,
+                                     workspace=None, stream=None):
+    """Packed NVFP4 paged forward; see ``msa_sparse_attention_nvfp4_paged`` in
+    include/msa.h. ``k`` .. ``v_scale`` are the views ``nvfp4_views`` returns.
+    Returns ``out`` or ``(out, lse)``."""
+    L = lib()
+    args, out, lse, _ = _fp4_args(q, k, k_scale, v, v_scale, q2k_indices, cu_seqlens_q,
+                                  page_table, seqused_k, k_global_scale, v_global_scale,
+                                  max_seqlen_q, softmax_scale, return_softmax_lse, out, lse,
+                                  workspace)
+    _check("msa_sparse_attention_nvfp4_paged",
+           L.msa_sparse_attention_nvfp4_paged(*args, _stream(stream)))
+    return (out, lse) if lse is not None else out
+
+
+class Nvfp4AttentionRunner(SparseAttentionRunner):
+    """The packed NVFP4 paged forward prepared once
+    (``msa_sparse_attention_nvfp4_prepare``) and launched by ``run()``."""
+
+    def __init__(self, q, k, k_scale, v, v_scale, q2k_indices, cu_seqlens_q, *, page_table,
+                 seqused_k, k_global_scale, v_global_scale, max_seqlen_q=None,
+                 softmax_scale=None, return_softmax_lse=False, out=None, lse=None,
+                 workspace=None):
+        L = lib()
+        args, self.out, self.lse, self.workspace = _fp4_args(
+            q, k, k_scale, v, v_scale, q2k_indices, cu_seqlens_q, page_table, seqused_k,
+            k_global_scale, v_global_scale, max_seqlen_q, softmax_scale, return_softmax_lse,
+            out, lse, workspace)
+        self._bound = (q, k, k_scale, v, v_scale, q2k_indices, cu_seqlens_q, page_table,
+                       seqused_k)
+        plan = C.c_void_p()
+        _check("msa_sparse_attention_nvfp4_prepare",
+               L.msa_sparse_attention_nvfp4_prepare(*args, C.byref(plan)))
+        self._plan = plan
+        self._lib = L
 
 
 def msa_proxy_score(q, k, cu_seqlens_q, cu_seqlens_k=None, *, causal=True, max_k_tiles=None,

@@ -5,6 +5,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <cmath>
 #include <mutex>
 #include <new>
 #include <tuple>
@@ -365,6 +366,8 @@ msa_status_t build_forward(
   if (!ok) return MSA_CUDA_ERROR;
   a.paged = paged ? 1 : 0;
   a.kv_fp8 = esize == 1 ? 1 : 0;
+  a.kv_fp4 = 0;
+  a.out_scale = 1.f;
   a.f16 = q_dtype == MSA_FP16 ? 1 : 0;
   a.cu_q = cu_seqlens_q;
   a.cu_k = cu_seqlens_k;
@@ -397,6 +400,46 @@ msa_status_t build_forward(
   a.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
   a.part_ml = reinterpret_cast<float*>(ws + L.off_part_ml);
   a.item_counter = u.item_counter;
+  return MSA_OK;
+}
+
+// The packed-NVFP4 paged route: the E4M3 kernel instance (converter warps),
+// fed by bulk copies of each page's K and V slices and block scales, with
+// the K global scale folded into the softmax scale and the V global scale
+// into the output.
+msa_status_t build_forward_fp4(
+    const void* q, msa_dtype_t q_dtype, const void* k, const void* k_scale, const void* v,
+    const void* v_scale, long long page_stride, float k_global_scale, float v_global_scale,
+    const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q, const int32_t* page_table,
+    int max_pages, int num_pages, const int32_t* seqused_k, int batch, int total_q,
+    int num_qo_heads, int num_kv_heads, int head_dim, int max_seqlen_q, float softmax_scale,
+    void* out, float* lse, void* workspace, size_t workspace_bytes, ForwardPlan* plan) {
+  if (k == nullptr || k_scale == nullptr || v == nullptr || v_scale == nullptr ||
+      page_table == nullptr)
+    return MSA_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(k_scale, 16) || !aligned(v, 16) || !aligned(v_scale, 16) ||
+      page_stride <= 0 || page_stride % 16 != 0)
+    return MSA_INVALID_ARG;
+  if (!(k_global_scale > 0.f) || !(v_global_scale > 0.f) || !std::isfinite(k_global_scale) ||
+      !std::isfinite(v_global_scale))
+    return MSA_INVALID_ARG;
+  if (q_dtype != MSA_BF16) return MSA_UNSUPPORTED;
+  // The checks and plan of the E4M3 paged route (the tensor maps it encodes
+  // over the code bytes are never used by this route).
+  const msa_status_t st = build_forward(
+      q, q_dtype, k, v, MSA_FP8_E4M3, q2k_indices, topk, cu_seqlens_q, nullptr, page_table,
+      max_pages, num_pages, seqused_k, batch, total_q, 0, num_qo_heads, num_kv_heads, head_dim,
+      max_seqlen_q, 1, softmax_scale, out, lse, workspace, workspace_bytes, plan);
+  if (st != MSA_OK || plan->empty) return st;
+  PrefillArgs& a = plan->a;
+  a.kv_fp4 = 1;
+  a.fp4_k = static_cast<const uint8_t*>(k);
+  a.fp4_k_scale = static_cast<const uint8_t*>(k_scale);
+  a.fp4_v = static_cast<const uint8_t*>(v);
+  a.fp4_v_scale = static_cast<const uint8_t*>(v_scale);
+  a.fp4_page_stride = page_stride;
+  a.scale_log2 *= k_global_scale;
+  a.out_scale = v_global_scale;
   return MSA_OK;
 }
 
@@ -468,6 +511,49 @@ msa_status_t msa_sparse_attention_run(const msa_attention_plan_t* plan, cudaStre
 void msa_sparse_attention_plan_free(msa_attention_plan_t* plan) { delete plan; }
 
 #undef MSA_FWD_ARGS
+
+#define MSA_FP4_ARGS                                                                        \
+  q, q_dtype, k, k_scale, v, v_scale, page_stride_bytes, k_global_scale, v_global_scale,  \
+      q2k_indices, topk, cu_seqlens_q, page_table, max_pages, num_pages, seqused_k, batch, \
+      total_q, num_qo_heads, num_kv_heads, head_dim, max_seqlen_q, softmax_scale, out, lse, \
+      workspace, workspace_bytes
+
+msa_status_t msa_sparse_attention_nvfp4_paged(
+    const void* q, msa_dtype_t q_dtype, const void* k, const void* k_scale, const void* v,
+    const void* v_scale, long long page_stride_bytes, float k_global_scale,
+    float v_global_scale, const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+    const int32_t* page_table, int max_pages, int num_pages, const int32_t* seqused_k,
+    int batch, int total_q, int num_qo_heads, int num_kv_heads, int head_dim,
+    int max_seqlen_q, float softmax_scale, void* out, float* lse, void* workspace,
+    size_t workspace_bytes, cudaStream_t stream) {
+  msa::ForwardPlan p;
+  const msa_status_t st = msa::build_forward_fp4(MSA_FP4_ARGS, &p);
+  if (st != MSA_OK) return st;
+  return msa::launch_forward(p, stream);
+}
+
+msa_status_t msa_sparse_attention_nvfp4_prepare(
+    const void* q, msa_dtype_t q_dtype, const void* k, const void* k_scale, const void* v,
+    const void* v_scale, long long page_stride_bytes, float k_global_scale,
+    float v_global_scale, const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+    const int32_t* page_table, int max_pages, int num_pages, const int32_t* seqused_k,
+    int batch, int total_q, int num_qo_heads, int num_kv_heads, int head_dim,
+    int max_seqlen_q, float softmax_scale, void* out, float* lse, void* workspace,
+    size_t workspace_bytes, msa_attention_plan_t** plan_out) {
+  if (plan_out == nullptr) return MSA_INVALID_ARG;
+  *plan_out = nullptr;
+  msa_attention_plan_t* plan = new (std::nothrow) msa_attention_plan_t;
+  if (plan == nullptr) return MSA_CUDA_ERROR;
+  const msa_status_t st = msa::build_forward_fp4(MSA_FP4_ARGS, &plan->p);
+  if (st != MSA_OK) {
+    delete plan;
+    return st;
+  }
+  *plan_out = plan;
+  return MSA_OK;
+}
+
+#undef MSA_FP4_ARGS
 
 
 

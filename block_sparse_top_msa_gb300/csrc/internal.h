@@ -53,8 +53,18 @@ struct PrefillArgs {
   CUtensorMap tmap_k;   // flat (d or d bytes, Hkv, Tk) / paged (.., 128, Hkv, pages)
   CUtensorMap tmap_v;
   int paged;
-  int kv_fp8;
+  int kv_fp8;           // E4M3 K/V, or packed NVFP4 K/V (kv_fp4), converted in the kernel
   int f16;              // q, k, v and out are fp16 (else bf16; E4M3 K/V only with bf16)
+  // Packed NVFP4 paged K/V: per page (fp4_page_stride bytes apart) and KV
+  // head, 128 x 64 bytes of E2M1 pairs and 128 x 8 E4M3 block scales for K
+  // (scales token-major) and for V (scales in 4 x 4 tiles, scale-index major).
+  int kv_fp4;
+  const uint8_t* fp4_k;
+  const uint8_t* fp4_k_scale;
+  const uint8_t* fp4_v;
+  const uint8_t* fp4_v_scale;
+  long long fp4_page_stride;
+  float out_scale;      // multiplies every output (the NVFP4 V global scale; else 1)
   const int32_t* cu_q;
   const int32_t* cu_k;
   const int32_t* page_table;

@@ -106,6 +106,7 @@ struct __align__(1024) PrefillSmem {
   uint64_t v_full[kVStages];
   uint64_t f8_full[kF8Stages];
   uint64_t f8_empty[kF8Stages];
+  int f8_valid[kF8Stages];  // NVFP4: the staged block's page is mapped (else it is zero)
   uint64_t qk_done[kSBuf];
   uint64_t p_full[kSBuf];
   uint64_t pv_done[kPV];
@@ -209,6 +210,77 @@ MSA_DEV void convert_tile(const uint8_t* src, uint8_t* dst_half0, int t) {
     e4m3x4_to_bf16(raw.y, outw[2], outw[3]);
     e4m3x4_to_bf16(raw.z, outw[4], outw[5]);
     e4m3x4_to_bf16(raw.w, outw[6], outw[7]);
+    uint8_t* dst = dst_half0 + (c >> 2) * kTile;
+    const int c16 = (c & 3) * 2;
+    *reinterpret_cast<uint4*>(dst + sw128_offset(r, c16)) =
+        make_uint4(outw[0], outw[1], outw[2], outw[3]);
+    *reinterpret_cast<uint4*>(dst + sw128_offset(r, c16 + 1)) =
+        make_uint4(outw[4], outw[5], outw[6], outw[7]);
+  }
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global to shared memory, completing on `bar`.
+MSA_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Bytes of one (page, KV head) slice of packed NVFP4: 128 tokens x 64 bytes of
+// E2M1 pairs, and 128 x 8 E4M3 block scales (one per 16 elements).
+constexpr uint32_t kFp4Data = 128 * 64;
+constexpr uint32_t kFp4Scales = 128 * 8;
+
+// Byte offset of token r's block scale s (0..7) in a slice's scale region:
+// token-major for K; for V, 4 x 4 tiles of (token, scale index) in row-major
+// tile order, each tile scale-index major.
+MSA_DEV int fp4_scale_offset(bool v_order, int r, int s) {
+  return v_order ? 32 * (r >> 2) + 16 * (s >> 2) + 4 * (s & 3) + (r & 3) : r * 8 + s;
+}
+
+// Sixteen E2M1 codes (eight bytes, element 2i in the low nibble of byte i)
+// times their E4M3 block scale, as eight packed bf16 pairs. Exact: E2M1 and
+// E4M3 are exact in f16, their product (at most 6 significant bits, magnitude
+// 2^-10 .. 2688) is exact in f16 and in bf16.
+MSA_DEV void fp4x16_to_bf16(uint2 codes, uint8_t scale, uint32_t (&out)[8]) {
+  uint32_t sc2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(sc2) : "h"((uint16_t)(scale | (scale << 8))));
+  const __half2 s2 = *reinterpret_cast<const __half2*>(&sc2);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t word = i < 4 ? codes.x : codes.y;
+    const uint16_t byte = (uint16_t)((word >> (8 * (i & 3))) & 0xFFu);
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(h2)
+        : "h"(byte));
+    const __half2 v2 = __hmul2(*reinterpret_cast<const __half2*>(&h2), s2);
+    const float2 f = __half22float2(v2);
+    out[i] = pack_bf16x2(f.x, f.y);
+  }
+}
+
+// Converts one staged NVFP4 slice (kFp4Data code bytes, then kFp4Scales
+// scales) into the two 64-column bf16 halves the MMA reads (SWIZZLE_128B
+// image), or writes zeros when the slice's page is unmapped.
+template <int kThreads>
+MSA_DEV void convert_fp4_tile(const uint8_t* src, bool v_order, bool valid, uint8_t* dst_half0,
+                              int t) {
+#pragma unroll 4
+  for (int j = 0; j < 1024 / kThreads; ++j) {
+    const int i = t + j * kThreads;
+    const int r = i >> 3, c = i & 7;  // token r, elements 16c .. 16c + 15
+    uint32_t outw[8];
+    if (valid) {
+      const uint2 codes = *reinterpret_cast<const uint2*>(src + r * 64 + c * 8);
+      fp4x16_to_bf16(codes, src[kFp4Data + fp4_scale_offset(v_order, r, c)], outw);
+    } else {
+#pragma unroll
+      for (int w = 0; w < 8; ++w) outw[w] = 0u;
+    }
     uint8_t* dst = dst_half0 + (c >> 2) * kTile;
     const int c16 = (c & 3) * 2;
     *reinterpret_cast<uint4*>(dst + sw128_offset(r, c16)) =
@@ -480,11 +552,30 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
               ok = false;
               break;
             }
-            mbar_expect_tx(&sm.f8_full[s8], 2 * kTile);
-            if (a.paged) {
+            if (a.kv_fp4) {
+              // Bulk copies of the page's K and V slices; an unmapped page is
+              // not read, and the converters write zeros for it.
+              const bool valid = page < a.num_pages;
+              sm.f8_valid[s8] = valid ? 1 : 0;
+              if (valid) {
+                const long long off = (long long)page * a.fp4_page_stride;
+                const size_t slice = (size_t)it.h * kFp4Data, sslice = (size_t)it.h * kFp4Scales;
+                uint8_t* kst = &sm.k8[s8][0];  // kTile bytes in the E4M3 instance
+                uint8_t* vst = &sm.v8[s8][0];
+                mbar_expect_tx(&sm.f8_full[s8], 2 * (kFp4Data + kFp4Scales));
+                bulk_load(kst, a.fp4_k + off + slice, kFp4Data, &sm.f8_full[s8]);
+                bulk_load(kst + kFp4Data, a.fp4_k_scale + off + sslice, kFp4Scales, &sm.f8_full[s8]);
+                bulk_load(vst, a.fp4_v + off + slice, kFp4Data, &sm.f8_full[s8]);
+                bulk_load(vst + kFp4Data, a.fp4_v_scale + off + sslice, kFp4Scales, &sm.f8_full[s8]);
+              } else {
+                mbar_arrive(&sm.f8_full[s8]);
+              }
+            } else if (a.paged) {
+              mbar_expect_tx(&sm.f8_full[s8], 2 * kTile);
               tma_load_4d(sm.k8[s8], &a.tmap_k, &sm.f8_full[s8], 0, 0, it.h, page);
               tma_load_4d(sm.v8[s8], &a.tmap_v, &sm.f8_full[s8], 0, 0, it.h, page);
             } else {
+              mbar_expect_tx(&sm.f8_full[s8], 2 * kTile);
               tma_load_3d(sm.k8[s8], &a.tmap_k, &sm.f8_full[s8], 0, it.h, row);
               tma_load_3d(sm.v8[s8], &a.tmap_v, &sm.f8_full[s8], 0, it.h, row);
             }
@@ -650,7 +741,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
           ok = false;
           break;
         }
-        convert_tile<R::kConvWarps * 32>(sm.k8[s8], sm.k[ks][0], ct);
+        const bool fp4_valid = a.kv_fp4 && sm.f8_valid[s8] != 0;
+        if (a.kv_fp4) convert_fp4_tile<R::kConvWarps * 32>(sm.k8[s8], false, fp4_valid, sm.k[ks][0], ct);
+        else convert_tile<R::kConvWarps * 32>(sm.k8[s8], sm.k[ks][0], ct);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.k_full[ks]);
@@ -658,7 +751,8 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
           ok = false;
           break;
         }
-        convert_tile<R::kConvWarps * 32>(sm.v8[s8], sm.v[vs][0], ct);
+        if (a.kv_fp4) convert_fp4_tile<R::kConvWarps * 32>(sm.v8[s8], true, fp4_valid, sm.v[vs][0], ct);
+        else convert_tile<R::kConvWarps * 32>(sm.v8[s8], sm.v[vs][0], ct);
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -860,7 +954,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       tc_fence_after();
       const size_t part = ((size_t)(it.tail < 0 ? 0 : it.tail) * a.splits + it.split) * a.rows_part;
       const bool has = lt > 0.f;
-      const float inv = has ? 1.f / lt : 0.f;
+      float os = 1.f;  // output scale (the NVFP4 V global scale)
+      if constexpr (FP8) os = a.out_scale;
+      const float inv = has ? os / lt : 0.f;
       auto store_half = [&](int half, const float* o) {
         if (!active) return;
         if (nsplit == 1) {
@@ -879,7 +975,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         } else {
           float4* dst = reinterpret_cast<float4*>(a.part_o + (part + row) * 128 + half * 64);
 #pragma unroll
-          for (int c = 0; c < 64; c += 4) dst[c >> 2] = make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+          for (int c = 0; c < 64; c += 4)
+            dst[c >> 2] = FP8 ? make_float4(o[c] * os, o[c + 1] * os, o[c + 2] * os, o[c + 3] * os)
+                              : make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
         }
       };
       // O is released (the next item's first PV may overwrite it) as soon as

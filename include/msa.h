@@ -152,6 +152,54 @@ msa_status_t msa_sparse_attention_run(const msa_attention_plan_t* plan, cudaStre
 void msa_sparse_attention_plan_free(msa_attention_plan_t* plan);
 
 /*
+ * Packed NVFP4 paged K/V forward ("flashinfer.msa_ops.msa_sparse_attention":
+ * the packed-NVFP4 paged route, parameters k, k_scale, v_scale,
+ * k_global_scale, v_global_scale, page_table, seqused_k;
+ * "prepare_msa_nvfp4_sparse_decode": k, k_scale, v_scale and the global
+ * scales). Computes what msa_sparse_attention_fwd computes (causal, paged)
+ * with K = e2m1 * block scale * k_global_scale and V = e2m1 * block scale *
+ * v_global_scale:
+ *   k, v          device uint8 views of a planar page pool: page p's slice for
+ *                 KV head h starts at p * page_stride_bytes + h * 8192 and holds
+ *                 128 tokens x 64 bytes of E2M1 pairs (element 2i in the low
+ *                 nibble of byte i, 2i + 1 in the high nibble);
+ *   k_scale,      device E4M3 block scales, one per 16 elements: (page, head)
+ *   v_scale       slice at p * page_stride_bytes + h * 1024, 128 x 8 bytes; K
+ *                 scales token-major (token t, scale s at 8 t + s), V scales in
+ *                 4 x 4 (token, scale) tiles, row-major over tiles, each tile
+ *                 scale-index major (t, s at 32 (t/4) + 16 (s/4) + 4 (s%4) +
+ *                 t%4). The pages' planar page is [K data | K scales | V data
+ *                 | V scales]; any stride multiple of 16 bytes is accepted;
+ *   k_global_scale, v_global_scale  positive, finite; the K one folds into the
+ *                 softmax scale, the V one into the output;
+ *   q             bf16 only; other arguments as msa_sparse_attention_fwd with
+ *                 cu_seqlens_k = NULL, causal = 1 and the workspace of
+ *                 msa_sparse_attention_workspace_size(..., paged = 1).
+ * Unmapped pages (page id outside [0, num_pages)) are neither read nor used.
+ * Returns MSA_INVALID_ARG for a NULL or misaligned pointer, a page stride not
+ * a positive multiple of 16, or a global scale that is not positive and
+ * finite; MSA_UNSUPPORTED for non-bf16 q; otherwise as the bf16 forward.
+ * msa_sparse_attention_nvfp4_prepare binds the same call into a plan that
+ * msa_sparse_attention_run launches (the pages' prepare / runner interface).
+ */
+msa_status_t msa_sparse_attention_nvfp4_paged(
+    const void* q, msa_dtype_t q_dtype, const void* k, const void* k_scale, const void* v,
+    const void* v_scale, long long page_stride_bytes, float k_global_scale,
+    float v_global_scale, const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+    const int32_t* page_table, int max_pages, int num_pages, const int32_t* seqused_k,
+    int batch, int total_q, int num_qo_heads, int num_kv_heads, int head_dim,
+    int max_seqlen_q, float softmax_scale, void* out, float* lse, void* workspace,
+    size_t workspace_bytes, cudaStream_t stream);
+msa_status_t msa_sparse_attention_nvfp4_prepare(
+    const void* q, msa_dtype_t q_dtype, const void* k, const void* k_scale, const void* v,
+    const void* v_scale, long long page_stride_bytes, float k_global_scale,
+    float v_global_scale, const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+    const int32_t* page_table, int max_pages, int num_pages, const int32_t* seqused_k,
+    int batch, int total_q, int num_qo_heads, int num_kv_heads, int head_dim,
+    int max_seqlen_q, float softmax_scale, void* out, float* lse, void* workspace,
+    size_t workspace_bytes, msa_attention_plan_t** plan);
+
+/*
  * Dense proxy pass, MSA stage 1 ("flashinfer.msa_ops.msa_proxy_score").
  *
  * output[h, t, q] = max over the keys j of KV block t of the UNSCALED logit

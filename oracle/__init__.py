@@ -19,7 +19,7 @@ from . import build as _build
 
 _lib = None
 
-BF16, FP16, E4M3 = 0, 1, 2
+BF16, FP16, E4M3, F64 = 0, 1, 2, 3
 
 
 def _load():
@@ -43,6 +43,9 @@ def _load():
             C.POINTER(C.c_uint32)]
         _lib.oracle_e4m3_decode.argtypes = [C.POINTER(C.c_uint8), C.c_longlong, f64p]
         _lib.oracle_bf16_decode.argtypes = [C.POINTER(C.c_uint16), C.c_longlong, f64p]
+        _lib.oracle_e2m1_decode.argtypes = [C.POINTER(C.c_uint8), C.c_longlong, f64p]
+        _lib.oracle_nvfp4_dequant.argtypes = [
+            C.POINTER(C.c_uint8), C.c_longlong, ci, ci, ci, C.c_double, C.c_double, f64p, f64p]
         for f in ("oracle_sparse_attention", "oracle_proxy_score", "oracle_topk_select",
                   "oracle_build_union"):
             getattr(_lib, f).restype = ci
@@ -57,8 +60,11 @@ def _raw(x):
     """Contiguous numpy view of the raw element bits of a CPU tensor/array.
 
     Returns (array, dtype code). bf16 and fp16 are passed as their 16-bit
-    patterns, E4M3 as bytes; the oracle decodes them itself.
+    patterns, E4M3 as bytes; the oracle decodes them itself. fp64 numpy
+    arrays (already decoded values, e.g. from ``nvfp4_dequant``) pass as is.
     """
+    if isinstance(x, np.ndarray) and x.dtype == np.float64:
+        return np.ascontiguousarray(x), F64
     try:
         import torch
     except ImportError:  # pragma: no cover
@@ -255,3 +261,37 @@ def bf16_decode(bits):
     out = np.zeros(a.shape, dtype=np.float64)
     lib.oracle_bf16_decode(_ptr(a, C.c_uint16), a.size, _ptr(out, C.c_double))
     return out
+
+
+def e2m1_decode(codes):
+    """Values of E2M1 codes (the low nibble of each byte)."""
+    lib = _load()
+    a = np.ascontiguousarray(np.asarray(codes, dtype=np.uint8))
+    out = np.zeros(a.shape, dtype=np.float64)
+    lib.oracle_e2m1_decode(_ptr(a, C.c_uint8), a.size, _ptr(out, C.c_double))
+    return out
+
+
+def nvfp4_dequant(pool, num_kv_heads, head_dim=128, k_global_scale=1.0, v_global_scale=1.0):
+    """fp64 K and V, (num_pages, Hkv, 128, d) each, of a planar NVFP4 page pool.
+
+    ``pool`` is (num_pages, page_stride) bytes; each page holds [K data | K
+    scales | V data | V scales] as "msa_sparse_attention" (k, k_scale, v_scale,
+    k_global_scale, v_global_scale) describes; see oracle_nvfp4_dequant for
+    the nibble and scale-order readings.
+    """
+    lib = _load()
+    try:
+        import torch
+        if isinstance(pool, torch.Tensor):
+            pool = pool.detach().cpu().contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(np.asarray(pool, dtype=np.uint8))
+    npg, stride = a.shape
+    kk = np.zeros((npg, num_kv_heads, 128, head_dim), dtype=np.float64)
+    vv = np.zeros_like(kk)
+    lib.oracle_nvfp4_dequant(_ptr(a, C.c_uint8), stride, npg, num_kv_heads, head_dim,
+                             float(k_global_scale), float(v_global_scale),
+                             _ptr(kk, C.c_double), _ptr(vv, C.c_double))
+    return kk, vv

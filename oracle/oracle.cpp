@@ -30,7 +30,15 @@
 //   R6 lse is the natural log of the sum of exp(scaled logits);
 //   R8 E4M3 is the "fn" variant: bias 7, no infinities, S.1111.111 is NaN;
 //   R9 the proxy block max runs over visible keys only, -inf when none;
-//   R11 a NaN score is never selected by top-k; ties go to the lower block id.
+//   R11 a NaN score is never selected by top-k; ties go to the lower block id;
+//   R12 packed NVFP4: element 2i of a row is the low nibble of byte i and
+//      element 2i + 1 the high nibble;
+//   R13 NVFP4 block scales: one E4M3 scale per 16 consecutive elements of a
+//      token's row; K scales linear (token-major); the V scales' "(4, 4)
+//      swizzle inside (token, scale index)" read as 4 x 4 tiles of (token,
+//      scale index) stored in row-major tile order, each tile scale-index
+//      major: (t, s) at byte 4 (d / 16) (t / 4) + 16 (s / 4) + 4 (s % 4) + t % 4
+//      of the (page, head)'s scale region (32 (t / 4) + ... for d = 128).
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -46,7 +54,7 @@ namespace {
 constexpr int kBlock = 128;  // KV block = page = 128 tokens (attention page, k parameter)
 constexpr double kNegInf = -std::numeric_limits<double>::infinity();
 
-enum { DT_BF16 = 0, DT_FP16 = 1, DT_E4M3 = 2 };
+enum { DT_BF16 = 0, DT_FP16 = 1, DT_E4M3 = 2, DT_F64 = 3 };
 
 // bf16 is the top half of an IEEE binary32.
 double bf16_value(uint16_t bits) {
@@ -78,10 +86,19 @@ double e4m3_value(uint8_t c) {
   return s ? -v : v;
 }
 
+// OCP FP4 E2M1, the element format of NVFP4: 1 sign, 2 exponent (bias 1),
+// 1 mantissa bit; exponent 0 is subnormal (m / 2); no infinities, no NaN.
+double e2m1_value(uint8_t c) {
+  const int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+  const double v = e == 0 ? 0.5 * m : std::ldexp(1.0 + 0.5 * m, e - 1);
+  return s ? -v : v;
+}
+
 double element(const void* base, int dtype, long long idx) {
   switch (dtype) {
     case DT_BF16: return bf16_value(static_cast<const uint16_t*>(base)[idx]);
     case DT_FP16: return fp16_value(static_cast<const uint16_t*>(base)[idx]);
+    case DT_F64: return static_cast<const double*>(base)[idx];
     default: return e4m3_value(static_cast<const uint8_t*>(base)[idx]);
   }
 }
@@ -166,6 +183,50 @@ void oracle_e4m3_decode(const uint8_t* codes, long long n, double* out) {
 
 void oracle_bf16_decode(const uint16_t* bits, long long n, double* out) {
   for (long long i = 0; i < n; ++i) out[i] = bf16_value(bits[i]);
+}
+
+// Decode n E2M1 codes (low nibble of each byte) to fp64.
+void oracle_e2m1_decode(const uint8_t* codes, long long n, double* out) {
+  for (long long i = 0; i < n; ++i) out[i] = e2m1_value(codes[i] & 15);
+}
+
+// NVFP4 paged K/V pool to fp64 K and V of shape (num_pages, Hkv, 128, d)
+// ("msa_sparse_attention": k, k_scale, v_scale, k_global_scale,
+// v_global_scale; "prepare_msa_nvfp4_sparse_decode": k, k_scale, v_scale).
+// Page p starts at byte p * page_stride and is planar:
+//   [K data (Hkv, 128, d/2) | K scales (Hkv, 128, d/16) | V data | V scales].
+// Value of element c of token t, head h: e2m1(nibble) * e4m3(its block
+// scale) * global scale (the K global scale folds into the softmax scale and
+// the V one into the output: the same product). Readings R12, R13.
+void oracle_nvfp4_dequant(const uint8_t* pool, long long page_stride, int num_pages, int Hkv,
+                          int d, double k_global, double v_global, double* k_out, double* v_out) {
+  const long long data = (long long)Hkv * kBlock * (d / 2);
+  const long long scales = (long long)Hkv * kBlock * (d / 16);
+  for (int p = 0; p < num_pages; ++p) {
+    const uint8_t* page = pool + (long long)p * page_stride;
+    for (int side = 0; side < 2; ++side) {
+      const uint8_t* dat = page + side * (data + scales);
+      const uint8_t* sc = dat + data;
+      const double global = side == 0 ? k_global : v_global;
+      double* dst = side == 0 ? k_out : v_out;
+      for (int h = 0; h < Hkv; ++h)
+        for (int t = 0; t < kBlock; ++t)
+          for (int c = 0; c < d; ++c) {
+            const uint8_t byte = dat[((long long)h * kBlock + t) * (d / 2) + c / 2];
+            const uint8_t code = (c % 2 == 0) ? (byte & 15) : (byte >> 4);
+            const int s = c / 16;
+            long long at;
+            if (side == 0) {
+              at = ((long long)h * kBlock + t) * (d / 16) + s;
+            } else {
+              at = (long long)h * kBlock * (d / 16) + 4 * (d / 16) * (t / 4) + 16 * (s / 4) +
+                   4 * (s % 4) + t % 4;
+            }
+            dst[(((long long)p * Hkv + h) * kBlock + t) * d + c] =
+                e2m1_value(code) * e4m3_value(sc[at]) * global;
+          }
+    }
+  }
 }
 
 // Sparse attention forward, plain definition ("msa_sparse_attention":

@@ -147,6 +147,45 @@ def test_forward_argument_errors(L):
     assert fwd(L, total_q=0) == 0                    # nothing to do, no launch
 
 
+def fp4(L, prepare=False, **kw):
+    args = dict(q=A, qdt=0, k=A, ks=A, v=A, vs=A, stride=36864, kgs=0.5, vgs=2.0, q2k=A, topk=16,
+                cu_q=A, pt=A, max_pages=4, num_pages=4, su=A, batch=1, total_q=4, hq=8, hkv=2,
+                d=128, max_sq=4, scale=0.0, out=A, lse=None, ws=A, ws_bytes=1 << 40)
+    args.update(kw)
+    vp = lambda x: None if x is None else C.c_void_p(x)
+    a = (vp(args["q"]), args["qdt"], vp(args["k"]), vp(args["ks"]), vp(args["v"]),
+         vp(args["vs"]), args["stride"], args["kgs"], args["vgs"], vp(args["q2k"]), args["topk"],
+         vp(args["cu_q"]), vp(args["pt"]), args["max_pages"], args["num_pages"], vp(args["su"]),
+         args["batch"], args["total_q"], args["hq"], args["hkv"], args["d"], args["max_sq"],
+         args["scale"], vp(args["out"]), vp(args["lse"]), vp(args["ws"]), args["ws_bytes"])
+    if prepare:
+        p = C.c_void_p(123)
+        st = L.msa_sparse_attention_nvfp4_prepare(*a, C.byref(p))
+        return st, p
+    return L.msa_sparse_attention_nvfp4_paged(*a, None)
+
+
+def test_nvfp4_argument_errors(L):
+    """The packed-NVFP4 paged route decides its argument errors on the host."""
+    assert fp4(L, ks=None) == 1 and fp4(L, vs=None) == 1 and fp4(L, k=None) == 1
+    assert fp4(L, pt=None) == 1                       # the route is paged only
+    assert fp4(L, su=None) == 1                       # paged length comes from seqused_k
+    assert fp4(L, ks=A + 8) == 1                      # 16-byte alignment of every view
+    assert fp4(L, stride=0) == 1 and fp4(L, stride=36872) == 1
+    assert fp4(L, kgs=0.0) == 1 and fp4(L, vgs=-1.0) == 1
+    assert fp4(L, kgs=float("inf")) == 1 and fp4(L, vgs=float("nan")) == 1
+    assert fp4(L, qdt=1) == 2                         # fp16 q: bf16 only on this route
+    assert fp4(L, d=64) == 2
+    assert fp4(L, ws_bytes=16) == 3                   # the paged workspace is still required
+    assert fp4(L, total_q=0) == 0                     # nothing to do, no launch
+    st, p = fp4(L, prepare=True, kgs=-2.0)
+    assert st == 1 and not p.value
+    st, p = fp4(L, prepare=True, total_q=0)
+    assert st == 0 and p.value
+    assert L.msa_sparse_attention_run(p, None) == 0   # empty plan: no launch
+    L.msa_sparse_attention_plan_free(p)
+
+
 def test_prepared_forward_host_paths(L):
     """prepare applies the forward's checks (and leaves no plan on failure);
     an empty problem gives a plan whose run launches nothing."""

@@ -357,6 +357,86 @@ def _decode_inputs(g, seqused, sq, hq, hkv, topk, npg_extra=3, dtype=torch.bfloa
                 seqused_k=torch.tensor(seqused, dtype=torch.int32))
 
 
+# ---------------------------------------------------------------- packed NVFP4 paged K/V
+# Global scales (K folds into the softmax scale, V into out), chosen so that
+# the decoded K and V have about unit RMS like the bf16 cases (the pool's
+# E2M1 x block-scale values have RMS about 5): the absolute output
+# tolerance assumes outputs of order one.
+NVFP4_KGS, NVFP4_VGS = 0.25, 0.125
+
+
+def _nvfp4_inputs(g, seqused, lens_q, hq, hkv, topk, bad_page=False):
+    cu_q = workloads.cu_from_lengths(lens_q)
+    pages = [(n + 127) // 128 for n in seqused]
+    npg = sum(pages) + 3
+    perm = torch.randperm(npg, generator=g).to(torch.int32)
+    pt = torch.zeros(len(seqused), max(pages) + 1, dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(pages):
+        pt[b, :n] = perm[off:off + n]
+        off += n
+    if bad_page:
+        pt[0, 1] = npg + 100  # unmapped: neither read nor attended
+    pool = workloads.nvfp4_pool(npg, hkv, g, "cpu")
+    q = torch.randn(int(cu_q[-1]), hq, 128, generator=g).to(torch.bfloat16)
+    q2k = workloads.select_blocks(workloads.query_positions(cu_q, seqused), hkv, topk, g)
+    return dict(q=q, pool=pool, q2k_indices=q2k, cu_seqlens_q=cu_q, page_table=pt,
+                seqused_k=torch.tensor(seqused, dtype=torch.int32)), npg
+
+
+def _nvfp4_run(msa, dev, hkv, runner=False):
+    k, ks, v, vs = msa.nvfp4_views(dev["pool"], hkv)
+    kw = dict(page_table=dev["page_table"], seqused_k=dev["seqused_k"],
+              k_global_scale=NVFP4_KGS, v_global_scale=NVFP4_VGS, return_softmax_lse=True)
+    if runner:
+        r = msa.Nvfp4AttentionRunner(dev["q"], k, ks, v, vs, dev["q2k_indices"],
+                                     dev["cu_seqlens_q"], **kw)
+        out, lse = r.run()
+        out, lse = out.clone(), lse.clone()
+        r.close()
+    else:
+        out, lse = msa.msa_sparse_attention_nvfp4_paged(dev["q"], k, ks, v, vs, dev["q2k_indices"],
+                                                        dev["cu_seqlens_q"], **kw)
+    torch.cuda.synchronize()
+    fault_clear(msa)
+    return out, lse
+
+
+NVFP4_CASES = [
+    # name, seqused, lens_q, hq, hkv, topk, bad_page
+    ("sq1_g16", [3000, 900, 129, 128, 4000], [1] * 5, 32, 2, 16, False),
+    ("sq4_g16_unmapped", [2000, 300, 130], [4] * 3, 32, 2, 16, True),
+    ("sq3_g4", [1500, 257, 10], [3, 3, 3], 8, 2, 5, False),
+    ("prefill_lq_le_lk", [700, 300], [40, 300], 8, 2, 6, True),
+]
+
+
+@pytest.mark.parametrize("case", NVFP4_CASES, ids=[c[0] for c in NVFP4_CASES])
+def test_nvfp4_paged_parity(msa, case):
+    """Packed NVFP4 paged K/V against the oracle on the decoded values (E2M1
+    nibbles x E4M3 block scales x global scales), decode and prefill shapes,
+    with an unmapped page."""
+    name, seqused, lens_q, hq, hkv, topk, bad = case
+    g = torch.Generator().manual_seed(len(name) * 31 + topk)
+    host, npg = _nvfp4_inputs(g, seqused, lens_q, hq, hkv, topk, bad_page=bad)
+    out, lse = _nvfp4_run(msa, to_dev(host, DEV), hkv)
+    kf, vf = oracle.nvfp4_dequant(host["pool"], hkv, 128, NVFP4_KGS, NVFP4_VGS)
+    ref_out, ref_lse = oracle.sparse_attention(
+        host["q"], kf, vf, host["q2k_indices"], host["cu_seqlens_q"], causal=True,
+        page_table=host["page_table"], seqused_k=host["seqused_k"], num_pages=npg)
+    check_attention(out, lse, ref_out, ref_lse, label=f"nvfp4_{name}")
+
+
+def test_nvfp4_runner_matches_forward(msa):
+    """The prepared NVFP4 forward (prepare once, run) gives the direct call's bits."""
+    g = torch.Generator().manual_seed(5)
+    host, _ = _nvfp4_inputs(g, [2500, 700, 129], [1, 1, 1], 32, 2, 16)
+    dev = to_dev(host, DEV)
+    o1, l1 = _nvfp4_run(msa, dev, 2)
+    o2, l2 = _nvfp4_run(msa, dev, 2, runner=True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 def test_decode_graph_replay(msa):
     """The forward is captured once into a CUDA graph with caller-owned out, lse
     and workspace and explicit sizes (no allocation, no host read-back); each

@@ -293,6 +293,81 @@ def test_e4m3_attention_uses_decoded_values():
     np.testing.assert_array_equal(l8, lb)
 
 
+def test_e2m1_decode_all_codes():
+    """The sixteen E2M1 codes (NVFP4 elements: sign, 2 exponent bits with bias
+    1, 1 mantissa bit, subnormal at exponent 0) decode to the format's values."""
+    want = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    got = oracle.e2m1_decode(np.arange(16, dtype=np.uint8))
+    np.testing.assert_array_equal(got[:8], want)
+    np.testing.assert_array_equal(got[8:], [-x for x in want])
+    assert np.signbit(got[8])  # code 8 is -0
+    # only the low nibble is a code
+    np.testing.assert_array_equal(oracle.e2m1_decode(np.array([0x37, 0xF7], dtype=np.uint8)),
+                                  [6.0, 6.0])
+
+
+def _nvfp4_offsets(hkv, d=128):
+    data, sc = hkv * 128 * d // 2, hkv * 128 * d // 16
+    return 0, data, data + sc, 2 * data + sc  # K data, K scales, V data, V scales
+
+
+def test_nvfp4_dequant_reads_nibbles_and_scales():
+    """Hand-placed bytes of a two-head planar page land where the reading puts
+    them: element 2i in the low nibble of byte i, K scales token-major, V
+    scales in scale-index-major 4 x 4 tiles, global scales multiplied in."""
+    hkv = 2
+    stride = workloads.nvfp4_page_stride(hkv)
+    kd, ks, vd, vs = _nvfp4_offsets(hkv)
+    pool = np.zeros((2, stride), dtype=np.uint8)
+    # K, page 1, head 1, token 5: byte 3 = 0x72 -> element 6 = code 2 (1.0), 7 = code 7 (6.0)
+    pool[1, kd + (1 * 128 + 5) * 64 + 3] = 0x72
+    pool[1, ks + (1 * 128 + 5) * 8 + 0] = 0x40          # E4M3 2.0 for elements 0..15
+    # V, page 0, head 0: every code 2 (1.0); one scale: token 6, scale index 5
+    pool[0, vd:vd + 128 * 64] = 0x22
+    pool[0, vs + 32 * (6 // 4) + 16 * (5 // 4) + 4 * (5 % 4) + 6 % 4] = 0x48  # E4M3 4.0
+    k, v = oracle.nvfp4_dequant(pool, hkv, 128, k_global_scale=0.5, v_global_scale=0.25)
+    assert k.shape == (2, hkv, 128, 128)
+    nz = np.argwhere(k != 0)
+    assert [tuple(x) for x in nz] == [(1, 1, 5, 6), (1, 1, 5, 7)]
+    assert k[1, 1, 5, 6] == 1.0 * 2.0 * 0.5 and k[1, 1, 5, 7] == 6.0 * 2.0 * 0.5
+    nz = np.argwhere(v != 0)
+    assert [tuple(x) for x in nz] == [(0, 0, 6, c) for c in range(80, 96)]
+    assert np.all(v[0, 0, 6, 80:96] == 1.0 * 4.0 * 0.25)
+    # the same scale byte read token-major would belong to token 6, scale 6
+    assert 32 * 1 + 16 * 1 + 4 * 1 + 2 != 6 * 8 + 5
+
+
+def test_nvfp4_attention_equals_attention_on_decoded_values():
+    """The NVFP4 route is attention over the decoded K and V: the oracle on the
+    fp64 decode equals the bf16 oracle on the same (exactly representable)
+    values, and the K global scale acts as a softmax-scale factor."""
+    g = torch.Generator().manual_seed(12)
+    hkv, hq, seqused, sq = 2, 8, [700, 300], 2
+    npg = sum((n + 127) // 128 for n in seqused) + 2
+    pool = workloads.nvfp4_pool(npg, hkv, g, "cpu")
+    perm = torch.randperm(npg, generator=g).to(torch.int32)
+    pt = torch.zeros(2, 6, dtype=torch.int32)
+    pt[0, :6], pt[1, :3] = perm[:6], perm[6:9]
+    cu = torch.tensor([0, sq, 2 * sq], dtype=torch.int32)
+    su = torch.tensor(seqused, dtype=torch.int32)
+    q = torch.randn(2 * sq, hq, 128, generator=g).to(torch.bfloat16)
+    q2k = workloads.select_blocks(workloads.query_positions(cu, seqused), hkv, 4, g)
+    k, v = oracle.nvfp4_dequant(pool, hkv, 128, k_global_scale=0.5, v_global_scale=0.25)
+    o4, l4 = oracle.sparse_attention(q, k, v, q2k, cu, page_table=pt, seqused_k=su, causal=True,
+                                     softmax_scale=0.1)
+    kb, vb = torch.from_numpy(k).to(torch.bfloat16), torch.from_numpy(v).to(torch.bfloat16)
+    assert np.array_equal(kb.double().numpy(), k) and np.array_equal(vb.double().numpy(), v)
+    ob, lb = oracle.sparse_attention(q, kb, vb, q2k, cu, page_table=pt, seqused_k=su, causal=True,
+                                     softmax_scale=0.1)
+    np.testing.assert_array_equal(o4, ob)
+    np.testing.assert_array_equal(l4, lb)
+    k1, _ = oracle.nvfp4_dequant(pool, hkv, 128, k_global_scale=1.0, v_global_scale=0.25)
+    o1, l1 = oracle.sparse_attention(q, k1, v, q2k, cu, page_table=pt, seqused_k=su, causal=True,
+                                     softmax_scale=0.05)
+    np.testing.assert_allclose(o1, o4, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l4, rtol=0, atol=1e-12)
+
+
 def test_proxy_closed_form():
     """q_h = (h+1) e0 and k_j[0] = j mod 128: the block max of (h+1)(j mod 128) is
     (h+1)*127 for a full visible block, (h+1)*(pos - 128 t) on the diagonal,

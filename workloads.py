@@ -56,6 +56,33 @@ def randn_chunked(shape, g, device, dtype):
     return out
 
 
+def nvfp4_page_stride(num_kv_heads: int, head_dim: int = 128) -> int:
+    """Bytes of one planar NVFP4 page: [K data | K scales | V data | V scales],
+    each (Hkv, 128, d/2) packed codes or (Hkv, 128, d/16) scales."""
+    return 2 * num_kv_heads * BLOCK * (head_dim // 2 + head_dim // 16)
+
+
+def nvfp4_pool(num_pages: int, num_kv_heads: int, g, device, head_dim: int = 128):
+    """A planar NVFP4 page pool (num_pages, page_stride) of uint8: uniform
+    random E2M1 nibbles and positive E4M3 block scales with exponent field
+    5..8 (2^-2 .. 2^1 times 1 + m/8), so no scale is zero, NaN or huge."""
+    stride = nvfp4_page_stride(num_kv_heads, head_dim)
+    pool = torch.empty((num_pages, stride), dtype=torch.uint8, device=device)
+    data = num_kv_heads * BLOCK * head_dim // 2
+    scales = num_kv_heads * BLOCK * head_dim // 16
+    per = max(1, (1 << 28) // stride)
+    for s in range(0, num_pages, per):
+        e = min(num_pages, s + per)
+        slab = pool[s:e]
+        slab.copy_(torch.randint(0, 256, (e - s, stride), generator=g, device=device,
+                                 dtype=torch.int32).to(torch.uint8))
+        for off in (data, 2 * data + scales):
+            ex = torch.randint(5, 9, (e - s, scales), generator=g, device=device, dtype=torch.int32)
+            ma = torch.randint(0, 8, (e - s, scales), generator=g, device=device, dtype=torch.int32)
+            slab[:, off:off + scales] = (ex * 8 + ma).to(torch.uint8)
+    return pool
+
+
 def cu_from_lengths(lengths: Sequence[int], device="cpu") -> torch.Tensor:
     cu = [0]
     for n in lengths:
@@ -173,6 +200,8 @@ class DecodeSpec:
     seqlen_q: int = 1
     head_dim: int = 128
     kv_dtype: str = "bf16"
+    k_global_scale: float = 1.0
+    v_global_scale: float = 1.0
 
 
 def make_decode(spec: DecodeSpec, seed: int, device="cpu", seqlen_q: Optional[int] = None):
@@ -198,9 +227,16 @@ def make_decode(spec: DecodeSpec, seed: int, device="cpu", seqlen_q: Optional[in
         off += n
     g = _gen(seed, device)
     d = spec.head_dim
-    kvdt = torch.float8_e4m3fn if spec.kv_dtype == "e4m3" else torch.bfloat16
-    k = randn_chunked((num_pages, spec.num_kv_heads, BLOCK, d), g, device, kvdt)
-    v = randn_chunked((num_pages, spec.num_kv_heads, BLOCK, d), g, device, kvdt)
+    extra = {}
+    if spec.kv_dtype == "nvfp4":
+        # K and V live in one planar page pool; k / v stay None.
+        k = v = None
+        extra = dict(kv_pool=nvfp4_pool(num_pages, spec.num_kv_heads, g, device, d),
+                     k_global_scale=spec.k_global_scale, v_global_scale=spec.v_global_scale)
+    else:
+        kvdt = torch.float8_e4m3fn if spec.kv_dtype == "e4m3" else torch.bfloat16
+        k = randn_chunked((num_pages, spec.num_kv_heads, BLOCK, d), g, device, kvdt)
+        v = randn_chunked((num_pages, spec.num_kv_heads, BLOCK, d), g, device, kvdt)
     q = randn_chunked((spec.batch * sq, spec.num_qo_heads, d), g, device, torch.bfloat16)
     cu_q = torch.arange(0, spec.batch * sq + 1, sq, dtype=torch.int32)
     pos = query_positions(cu_q, seqused.tolist())
@@ -208,7 +244,7 @@ def make_decode(spec: DecodeSpec, seed: int, device="cpu", seqlen_q: Optional[in
     q2k = select_blocks(pos, spec.num_kv_heads, spec.topk, gs)
     return dict(q=q, k=k, v=v, q2k_indices=q2k.to(device), cu_seqlens_q=cu_q.to(device),
                 page_table=page_table.to(device), seqused_k=seqused.to(torch.int32).to(device),
-                causal=True, softmax_scale=d ** -0.5, seqlen_q=sq, num_pages=num_pages)
+                causal=True, softmax_scale=d ** -0.5, seqlen_q=sq, num_pages=num_pages, **extra)
 
 
 # --------------------------------------------------------------------------
@@ -251,6 +287,9 @@ MIXED_E4M3 = PrefillSpec("e4m3kv_varlen_prefill_8xU[4096,65536]_h32kv4_top16", N
                          kv_dtype="e4m3", draw_lengths=(8, 4096, 65536))
 PAGED_DECODE = DecodeSpec("paged_decode_b128_U[8192,131072]_h64kv4_top16", 128, (8192, 131072),
                           64, 4, 16)
+PAGED_DECODE_NVFP4 = DecodeSpec("nvfp4_paged_decode_b128_U[8192,131072]_h64kv4_top16", 128,
+                                (8192, 131072), 64, 4, 16, kv_dtype="nvfp4",
+                                k_global_scale=0.5, v_global_scale=2.0)
 TWO_STAGE = TwoStageSpec("two_stage_proxy_top16_attn_1x65536_h32kv4", [65536], 32, 32, 4, 16)
 
 
