@@ -83,7 +83,7 @@ def barrier(world):
 # build that was captured; otherwise the roofline's "traffic" is null.
 TRAFFIC_SOURCES = ("prefill.cu", "common.cuh", "tmem_wide.cuh", "internal.h", "tmap.h", "api.cu",
                    "union.cu", "tile_map.cuh")
-TRAFFIC_MEASURED = {"fingerprint": "fb604c52b1973da9", "bytes_per_launch": 2.426e9,
+TRAFFIC_MEASURED = {"fingerprint": "2e9fd8d5106ae727", "bytes_per_launch": 2.427e9,
                     "profile": "profiles/prefill_kernel_flat_varlen_2x32768_traffic.md"}
 
 
@@ -229,7 +229,7 @@ def run_prefill(msa, inp, out, lse, ws, max_sq):
         max_seqlen_q=max_sq, out=out, lse=lse, workspace=ws)
 
 
-def cpu_baseline_prefill(inp, rows_target=512, threads=None):
+def cpu_baseline_prefill(inp, rows_target=3072, threads=None):
     """fp64 oracle on a bounded row sample; returns (TFLOP/s, cores, sample, seconds)."""
     import oracle
     cpu = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp.items()}
