@@ -93,6 +93,43 @@ def test_decode_workload(msa, sq):
     check_attention(out, lse, ref_out, ref_lse, label=f"{spec.name}_sq{sq}")
 
 
+@pytest.mark.parametrize("sq", [1, 4])
+def test_nvfp4_decode_workload(msa, sq):
+    """The packed NVFP4 paged decode at its benchmark size, in the benchmark's
+    launch configuration; every query row of a sample of requests (every
+    16th) is compared with every head. The oracle decodes only the pages
+    those rows can read (renumbered into a compact pool)."""
+    spec = workloads.PAGED_DECODE_NVFP4
+    g = workloads.make_decode(spec, seed=0, device=DEV, seqlen_q=sq)
+    q2k, pt, cu = g["q2k_indices"], g["page_table"], g["cu_seqlens_q"]
+    hkv = q2k.shape[0]
+    k, ks, v, vs = msa.nvfp4_views(g["kv_pool"], hkv)
+    out, lse = msa.msa_sparse_attention_nvfp4_paged(
+        g["q"], k, ks, v, vs, q2k, cu, page_table=pt, seqused_k=g["seqused_k"],
+        k_global_scale=spec.k_global_scale, v_global_scale=spec.v_global_scale, max_seqlen_q=sq,
+        return_softmax_lse=True)
+    torch.cuda.synchronize()
+    fault_clear(msa)
+    B = pt.shape[0]
+    reqs = torch.arange(0, B, 16, device=pt.device)
+    rows = (reqs[:, None] * sq + torch.arange(sq, device=pt.device)).flatten()
+    ids = q2k[:, rows, :].long()
+    req = (rows // sq)[None, :, None].expand_as(ids)
+    ok = (ids >= 0) & (ids < pt.shape[1])
+    pages = pt[req[ok], ids[ok]].long()
+    npg = g["kv_pool"].shape[0]
+    used = torch.unique(pages[(pages >= 0) & (pages < npg)])
+    remap = torch.full((npg,), used.numel(), dtype=torch.int32, device=pt.device)
+    remap[used] = torch.arange(used.numel(), dtype=torch.int32, device=pt.device)
+    pool = g["kv_pool"].index_select(0, used).cpu()
+    kf, vf = oracle.nvfp4_dequant(pool, hkv, 128, spec.k_global_scale, spec.v_global_scale)
+    ref_out, ref_lse = oracle.sparse_attention(
+        g["q"].cpu(), kf, vf, q2k.cpu(), cu.cpu(), causal=True,
+        softmax_scale=f32(g["softmax_scale"]), page_table=remap[pt.long()].cpu(),
+        seqused_k=g["seqused_k"].cpu(), num_pages=used.numel(), rows=rows.to(torch.int32).cpu())
+    check_attention(out, lse, ref_out, ref_lse, rows=rows.cpu(), label=f"{spec.name}_sq{sq}")
+
+
 def test_two_stage_workload(msa):
     spec = workloads.TWO_STAGE
     g = workloads.make_two_stage(spec, seed=0, device=DEV)

@@ -287,9 +287,12 @@ MIXED_E4M3 = PrefillSpec("e4m3kv_varlen_prefill_8xU[4096,65536]_h32kv4_top16", N
                          kv_dtype="e4m3", draw_lengths=(8, 4096, 65536))
 PAGED_DECODE = DecodeSpec("paged_decode_b128_U[8192,131072]_h64kv4_top16", 128, (8192, 131072),
                           64, 4, 16)
+# Global scales chosen so that the decoded K and V have about unit RMS (the
+# pool's E2M1 x block-scale values have RMS about 5), like the N(0,1) values
+# of the other workloads.
 PAGED_DECODE_NVFP4 = DecodeSpec("nvfp4_paged_decode_b128_U[8192,131072]_h64kv4_top16", 128,
                                 (8192, 131072), 64, 4, 16, kv_dtype="nvfp4",
-                                k_global_scale=0.5, v_global_scale=2.0)
+                                k_global_scale=0.25, v_global_scale=0.125)
 TWO_STAGE = TwoStageSpec("two_stage_proxy_top16_attn_1x65536_h32kv4", [65536], 32, 32, 4, 16)
 
 
