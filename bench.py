@@ -516,6 +516,65 @@ def bench_decode_nvfp4(msa, device, flush, seed=0, sqs=(1, 4), reps=7):
     return out
 
 
+def bench_nvfp4_prefill(msa, device, flush, seed=0, reps=3):
+    """Paged prefill over a planar NVFP4 pool, on both routes: the default one
+    (bf16 page pool decoded once per call, then the bf16 attention kernel) and
+    the in-kernel decode (paged workspace size only)."""
+    spec = workloads.PAGED_PREFILL_NVFP4
+    inp = workloads.make_paged_prefill_nvfp4(spec, seed, device=device)
+    q, q2k, cu, pt = inp["q"], inp["q2k_indices"], inp["cu_seqlens_q"], inp["page_table"]
+    tq, hq, _ = q.shape
+    hkv = q2k.shape[0]
+    G = hq // hkv
+    max_sq = max(inp["lengths"])
+    cnt = visible_counts(q2k, cu, inp["lengths"])
+    flops = 4.0 * D * G * float(cnt.sum())
+    kk, ks, vv, vs = msa.nvfp4_views(inp["kv_pool"], hkv)
+    out = torch.empty_like(q)
+    lse = torch.empty((tq, hq), dtype=torch.float32, device=device)
+    pk = peaks()
+    B = pt.shape[0]
+    sizes = {
+        "bf16_pool": msa.msa_sparse_attention_nvfp4_workspace_size(B, tq, hq, hkv, D, spec.topk,
+                                                                   max_sq, pt.shape[1]),
+        "in_kernel": msa.msa_sparse_attention_workspace_size(B, tq, hq, hkv, D, spec.topk, max_sq,
+                                                             True)}
+    res = {"workload": spec.name, "tokens": int(tq)}
+    for route, need in sizes.items():
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+
+        def call():
+            msa.msa_sparse_attention_nvfp4_paged(
+                q, kk, ks, vv, vs, q2k, cu, page_table=pt, seqused_k=inp["seqused_k"],
+                k_global_scale=inp["k_global_scale"], v_global_scale=inp["v_global_scale"],
+                max_seqlen_q=max_sq, out=out, lse=lse, workspace=ws)
+
+        for _ in range(2):
+            call()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        ts, ta = [], []
+        for _ in range(reps):
+            flush.fill_(1)
+            msa.msa_set_timing_events(ev)
+            call()
+            ev[2].synchronize()
+            ts.append(ev[0].elapsed_time(ev[2]) * 1e-3)
+            ta.append(ev[1].elapsed_time(ev[2]) * 1e-3)
+        msa.msa_set_timing_events(None)
+        t, t_attn = statistics.median(ts), statistics.median(ta)
+        res[route] = {
+            "value": round(flops / t / 1e12, 2), "unit": "TFLOP/s", "ms": round(t * 1e3, 3),
+            "attention_ms": round(t_attn * 1e3, 3),
+            "roofline": {"bound": "tensor", "achieved": round(flops / t_attn / 1e12, 2),
+                         "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                         "frac": round(flops / t_attn / 1e12 / pk["bf16_sus"], 4)}}
+        del ws
+    res["value"], res["unit"] = res["bf16_pool"]["value"], "TFLOP/s"
+    del inp
+    torch.cuda.empty_cache()
+    return res
+
+
 def bench_decode_proxy(msa, inp, flush, pk, reps):
     """Paged proxy scores (reduce_heads) of the decode batch: every key of every
     request is visible to its one query token, so the kernel streams the whole
@@ -742,7 +801,8 @@ def main():
     if args.profile_nvfp4:
         flush = l2_flush_buffer(device)
         print(json.dumps({"profile_nvfp4": bench_decode_nvfp4(msa, device, flush,
-                                                              reps=args.steps)}))
+                                                              reps=args.steps),
+                          "profile_nvfp4_prefill": bench_nvfp4_prefill(msa, device, flush)}))
         return 0
     if args.profile_e4m3:
         flush = l2_flush_buffer(device)
@@ -764,6 +824,8 @@ def main():
         secondary["decode"] = bench_decode(msa, device, flush)
         torch.cuda.empty_cache()
         secondary["decode_nvfp4"] = bench_decode_nvfp4(msa, device, flush)
+        torch.cuda.empty_cache()
+        secondary["prefill_nvfp4"] = bench_nvfp4_prefill(msa, device, flush)
         torch.cuda.empty_cache()
         secondary["two_stage"] = bench_two_stage(msa, device, flush)
         torch.cuda.empty_cache()

@@ -56,6 +56,8 @@ def lib():
         L.msa_sparse_attention_workspace_size.argtypes = [i32] * 8
         L.msa_sparse_attention_workspace_size_kv.restype = sz
         L.msa_sparse_attention_workspace_size_kv.argtypes = [i32] * 10
+        L.msa_sparse_attention_nvfp4_workspace_size.restype = sz
+        L.msa_sparse_attention_nvfp4_workspace_size.argtypes = [i32] * 8
         L.msa_sparse_attention_fwd.restype = i32
         L.msa_sparse_attention_fwd.argtypes = [
             vp, i32, vp, vp, i32, vp, i32, vp, vp, vp, i32, i32, vp, i32, i32, i32, i32, i32,
@@ -165,6 +167,12 @@ def msa_sparse_attention_workspace_size_kv(batch, total_q, num_qo_heads, num_kv_
         code, total_k))
 
 
+def msa_sparse_attention_nvfp4_workspace_size(batch, total_q, num_qo_heads, num_kv_heads,
+                                              head_dim, topk, max_seqlen_q, max_pages) -> int:
+    return int(lib().msa_sparse_attention_nvfp4_workspace_size(
+        batch, total_q, num_qo_heads, num_kv_heads, head_dim, topk, max_seqlen_q, max_pages))
+
+
 def msa_sparse_attention_fwd(q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k=None, *,
                              causal=False, softmax_scale=None, page_table=None, seqused_k=None,
                              max_seqlen_q=None, return_softmax_lse=False, out=None, lse=None,
@@ -206,9 +214,9 @@ def _forward_args(q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k, causal, soft
     if lse is None and return_softmax_lse:
         lse = torch.empty((total_q, hq), dtype=torch.float32, device=q.device)
     if workspace is None:
-        need = msa_sparse_attention_workspace_size_kv(batch, total_q, hq, hkv, d, topk,
-                                                      max(1, max_seqlen_q), paged, _dtype_code(k),
-                                                      0 if paged else k.shape[0])
+        need = msa_sparse_attention_workspace_size_kv(
+            batch, total_q, hq, hkv, d, topk, max(1, max_seqlen_q), paged, _dtype_code(k),
+            page_table.shape[1] if paged else k.shape[0])
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     args = (_p(q), _dtype_code(q), _p(k), _p(v), _dtype_code(k), _p(q2k_indices), topk,
             _p(cu_seqlens_q), _p(cu_seqlens_k), _p(page_table),
@@ -298,8 +306,8 @@ def _fp4_args(q, k, k_scale, v, v_scale, q2k_indices, cu_seqlens_q, page_table, 
     if lse is None and return_softmax_lse:
         lse = torch.empty((total_q, hq), dtype=torch.float32, device=q.device)
     if workspace is None:
-        need = msa_sparse_attention_workspace_size(batch, total_q, hq, hkv, d, topk,
-                                                   max(1, max_seqlen_q), True)
+        need = msa_sparse_attention_nvfp4_workspace_size(batch, total_q, hq, hkv, d, topk,
+                                                         max(1, max_seqlen_q), page_table.shape[1])
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     args = (_p(q), _dtype_code(q), _p(k), _p(k_scale), _p(v), _p(v_scale), stride,
             float(k_global_scale), float(v_global_scale), _p(q2k_indices), topk, _p(cu_seqlens_q),

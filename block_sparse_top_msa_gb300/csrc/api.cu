@@ -151,6 +151,32 @@ size_t kv_copy_bytes(long long total_k, int hkv) {
   return up256((size_t)total_k * (size_t)hkv * 128 * 2);
 }
 
+// Paged E4M3 / NVFP4 K/V on a prefill-sized call (query rows x query heads at
+// least the page table's key capacity x KV heads) is decoded into a bf16 page
+// pool (batch * max_pages pages) with a renumbered page table, for the same
+// reason as the flat copy above.
+bool paged_copy_route(long long total_q, int hq, int batch, int max_pages, int hkv) {
+  return batch > 0 && max_pages > 0 &&
+         total_q * hq >= (long long)batch * max_pages * 128 * hkv;
+}
+// Bytes of the bf16 K and V page pools and the renumbered table.
+size_t page_pool_bytes(int batch, int max_pages, int hkv) {
+  const size_t pages = (size_t)batch * max_pages;
+  return 2 * up256(pages * hkv * 128 * 128 * 2) + up256(pages * sizeof(int32_t));
+}
+// Places the pools after the first `need` bytes of the workspace.
+void place_page_pool(PageDecodeArgs* pd, uint8_t* ws, size_t need, int batch, int max_pages,
+                     int hkv) {
+  const size_t pages = (size_t)batch * max_pages;
+  const size_t side = up256(pages * hkv * 128 * 128 * 2);
+  pd->k16 = reinterpret_cast<uint16_t*>(ws + need);
+  pd->v16 = reinterpret_cast<uint16_t*>(ws + need + side);
+  pd->pt_out = reinterpret_cast<int32_t*>(ws + need + 2 * side);
+  pd->batch = batch;
+  pd->max_pages = max_pages;
+  pd->hkv = hkv;
+}
+
 // (d, H, T) map over a (T, H, d) tensor; element size 2 (bf16) or 1 (e4m3).
 bool map_rows(CUtensorMap* m, const void* base, int esize, int H, long long T, uint32_t box_h,
               uint32_t box_t) {
@@ -253,9 +279,25 @@ size_t msa_sparse_attention_workspace_size_kv(int batch, int total_q, int num_qo
   const size_t base = msa_sparse_attention_workspace_size(
       batch, total_q, num_qo_heads, num_kv_heads, head_dim, topk, max_seqlen_q, paged);
   if (base == 0 || total_k < 0) return 0;
+  if (paged != 0) {  // total_k carries the page table width
+    if (kv_dtype != MSA_FP8_E4M3 || !paged_copy_route(total_q, num_qo_heads, batch, total_k,
+                                                      num_kv_heads))
+      return base;
+    return base + page_pool_bytes(batch, total_k, num_kv_heads);
+  }
   if (!kv_decode_route(kv_dtype, paged != 0, total_q, num_qo_heads, total_k, num_kv_heads))
     return base;
   return base + 2 * kv_copy_bytes(total_k, num_kv_heads);
+}
+
+size_t msa_sparse_attention_nvfp4_workspace_size(int batch, int total_q, int num_qo_heads,
+                                                 int num_kv_heads, int head_dim, int topk,
+                                                 int max_seqlen_q, int max_pages) {
+  const size_t base = msa_sparse_attention_workspace_size(
+      batch, total_q, num_qo_heads, num_kv_heads, head_dim, topk, max_seqlen_q, 1);
+  if (base == 0 || max_pages < 1) return 0;
+  if (!paged_copy_route(total_q, num_qo_heads, batch, max_pages, num_kv_heads)) return base;
+  return base + page_pool_bytes(batch, max_pages, num_kv_heads);
 }
 
 }  // extern "C"
@@ -266,7 +308,8 @@ namespace {
 // Everything a forward launch needs, decided and encoded on the host.
 struct ForwardPlan {
   bool empty = true;  // total_q == 0: nothing to launch
-  KvDecodeArgs dq{};  // n16 > 0: E4M3 K/V decoded to bf16 before the union kernel
+  KvDecodeArgs dq{};    // n16 > 0: E4M3 K/V decoded to bf16 before the union kernel
+  PageDecodeArgs pd{};  // mode > 0: paged E4M3 / NVFP4 pages decoded to a bf16 pool first
   UnionArgs u{};
   PrefillArgs a{};
 };
@@ -328,6 +371,22 @@ msa_status_t build_forward(
     k = plan->dq.k16;
     v = plan->dq.v16;
     kv_dtype = MSA_BF16;
+  } else if (kv_dtype == MSA_FP8_E4M3 && paged &&
+             paged_copy_route(total_q, num_qo_heads, batch, max_pages, num_kv_heads) &&
+             workspace_bytes >= need + page_pool_bytes(batch, max_pages, num_kv_heads)) {
+    PageDecodeArgs& pd = plan->pd;
+    place_page_pool(&pd, ws, need, batch, max_pages, num_kv_heads);
+    pd.mode = 1;
+    pd.page_table = page_table;
+    pd.seqused_k = seqused_k;
+    pd.num_pages = num_pages;
+    pd.k8 = static_cast<const uint8_t*>(k);
+    pd.v8 = static_cast<const uint8_t*>(v);
+    k = pd.k16;
+    v = pd.v16;
+    kv_dtype = MSA_BF16;
+    page_table = pd.pt_out;
+    num_pages = batch * max_pages;
   }
   const int esize = kv_dtype == MSA_FP8_E4M3 ? 1 : 2;
 
@@ -424,6 +483,36 @@ msa_status_t build_forward_fp4(
       !std::isfinite(v_global_scale))
     return MSA_INVALID_ARG;
   if (q_dtype != MSA_BF16) return MSA_UNSUPPORTED;
+  // Prefill-sized calls given the larger workspace: decode the pages into a
+  // bf16 pool and run the bf16 attention kernel on it.
+  const size_t need = msa_sparse_attention_workspace_size(
+      batch, total_q, num_qo_heads, num_kv_heads, head_dim, topk, max_seqlen_q, 1);
+  if (need > 0 && total_q > 0 && workspace != nullptr && aligned(workspace, 256) &&
+      paged_copy_route(total_q, num_qo_heads, batch, max_pages, num_kv_heads) &&
+      workspace_bytes >= need + page_pool_bytes(batch, max_pages, num_kv_heads)) {
+    PageDecodeArgs pd{};
+    place_page_pool(&pd, static_cast<uint8_t*>(workspace), need, batch, max_pages,
+                    num_kv_heads);
+    pd.mode = 2;
+    pd.page_table = page_table;
+    pd.seqused_k = seqused_k;
+    pd.num_pages = num_pages;
+    pd.fp4_k = static_cast<const uint8_t*>(k);
+    pd.fp4_k_scale = static_cast<const uint8_t*>(k_scale);
+    pd.fp4_v = static_cast<const uint8_t*>(v);
+    pd.fp4_v_scale = static_cast<const uint8_t*>(v_scale);
+    pd.fp4_page_stride = page_stride;
+    const msa_status_t sc = build_forward(
+        q, q_dtype, pd.k16, pd.v16, MSA_BF16, q2k_indices, topk, cu_seqlens_q, nullptr,
+        pd.pt_out, max_pages, batch * max_pages, seqused_k, batch, total_q, 0, num_qo_heads,
+        num_kv_heads, head_dim, max_seqlen_q, 1, softmax_scale, out, lse, workspace,
+        workspace_bytes, plan);
+    if (sc != MSA_OK || plan->empty) return sc;
+    plan->pd = pd;
+    plan->a.scale_log2 *= k_global_scale;
+    plan->a.out_scale = v_global_scale;
+    return MSA_OK;
+  }
   // The checks and plan of the E4M3 paged route (the tensor maps it encodes
   // over the code bytes are never used by this route).
   const msa_status_t st = build_forward(
@@ -447,6 +536,8 @@ msa_status_t launch_forward(const ForwardPlan& p, cudaStream_t stream) {
   if (p.empty) return MSA_OK;
   mark(0, stream);
   cudaError_t e = launch_kv_decode(p.dq, stream);
+  if (e != cudaSuccess) return MSA_CUDA_ERROR;
+  e = launch_page_decode(p.pd, stream);
   if (e != cudaSuccess) return MSA_CUDA_ERROR;
   e = launch_build_union(p.u, stream);
   if (e != cudaSuccess) return MSA_CUDA_ERROR;

@@ -264,6 +264,40 @@ MSA_DEV void e4m3x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
   }
 }
 
+// Bytes of one (page, KV head) slice of packed NVFP4: 128 tokens x 64 bytes of
+// E2M1 pairs, and 128 x 8 E4M3 block scales (one per 16 elements).
+constexpr uint32_t kFp4Data = 128 * 64;
+constexpr uint32_t kFp4Scales = 128 * 8;
+
+// Byte offset of token r's block scale s (0..7) in a slice's scale region:
+// token-major for K; for V, 4 x 4 tiles of (token, scale index) in row-major
+// tile order, each tile scale-index major.
+MSA_DEV int fp4_scale_offset(bool v_order, int r, int s) {
+  return v_order ? 32 * (r >> 2) + 16 * (s >> 2) + 4 * (s & 3) + (r & 3) : r * 8 + s;
+}
+
+// Sixteen E2M1 codes (eight bytes, element 2i in the low nibble of byte i)
+// times their E4M3 block scale, as eight packed bf16 pairs. Exact: E2M1 and
+// E4M3 are exact in f16, their product (at most 6 significant bits, magnitude
+// 2^-10 .. 2688) is exact in f16 and in bf16.
+MSA_DEV void fp4x16_to_bf16(uint2 codes, uint8_t scale, uint32_t (&out)[8]) {
+  uint32_t sc2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(sc2) : "h"((uint16_t)(scale | (scale << 8))));
+  const __half2 s2 = *reinterpret_cast<const __half2*>(&sc2);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t word = i < 4 ? codes.x : codes.y;
+    const uint16_t byte = (uint16_t)((word >> (8 * (i & 3))) & 0xFFu);
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(h2)
+        : "h"(byte));
+    const __half2 v2 = __hmul2(*reinterpret_cast<const __half2*>(&h2), s2);
+    const float2 f = __half22float2(v2);
+    out[i] = pack_bf16x2(f.x, f.y);
+  }
+}
+
 // Byte offset of the 16-byte chunk `c16` (0..7) of row `row` inside a
 // 128-byte-swizzled tile whose rows are 128 bytes (the TMA SWIZZLE_128B image).
 MSA_DEV uint32_t sw128_offset(uint32_t row, uint32_t c16) {

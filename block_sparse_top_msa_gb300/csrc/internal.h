@@ -149,4 +149,25 @@ struct KvDecodeArgs {
 };
 cudaError_t launch_kv_decode(const KvDecodeArgs& a, cudaStream_t s);
 
+// Paged E4M3 (mode 1: (pages, Hkv, 128, 128) bytes) or packed NVFP4 (mode 2:
+// planar pages) K/V decoded into a bf16 pool of batch * max_pages pages, with
+// the renumbered page table written to pt_out (batch, max_pages).
+struct PageDecodeArgs {
+  int mode = 0;  // 0: nothing to do
+  const int32_t* page_table = nullptr;
+  const int32_t* seqused_k = nullptr;
+  int max_pages = 0, num_pages = 0, batch = 0, hkv = 0;
+  const uint8_t* k8 = nullptr;
+  const uint8_t* v8 = nullptr;
+  const uint8_t* fp4_k = nullptr;
+  const uint8_t* fp4_k_scale = nullptr;
+  const uint8_t* fp4_v = nullptr;
+  const uint8_t* fp4_v_scale = nullptr;
+  long long fp4_page_stride = 0;
+  uint16_t* k16 = nullptr;
+  uint16_t* v16 = nullptr;
+  int32_t* pt_out = nullptr;
+};
+cudaError_t launch_page_decode(const PageDecodeArgs& a, cudaStream_t s);
+
 }  // namespace msa

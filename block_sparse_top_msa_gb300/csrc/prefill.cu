@@ -229,40 +229,6 @@ MSA_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar
       : "memory");
 }
 
-// Bytes of one (page, KV head) slice of packed NVFP4: 128 tokens x 64 bytes of
-// E2M1 pairs, and 128 x 8 E4M3 block scales (one per 16 elements).
-constexpr uint32_t kFp4Data = 128 * 64;
-constexpr uint32_t kFp4Scales = 128 * 8;
-
-// Byte offset of token r's block scale s (0..7) in a slice's scale region:
-// token-major for K; for V, 4 x 4 tiles of (token, scale index) in row-major
-// tile order, each tile scale-index major.
-MSA_DEV int fp4_scale_offset(bool v_order, int r, int s) {
-  return v_order ? 32 * (r >> 2) + 16 * (s >> 2) + 4 * (s & 3) + (r & 3) : r * 8 + s;
-}
-
-// Sixteen E2M1 codes (eight bytes, element 2i in the low nibble of byte i)
-// times their E4M3 block scale, as eight packed bf16 pairs. Exact: E2M1 and
-// E4M3 are exact in f16, their product (at most 6 significant bits, magnitude
-// 2^-10 .. 2688) is exact in f16 and in bf16.
-MSA_DEV void fp4x16_to_bf16(uint2 codes, uint8_t scale, uint32_t (&out)[8]) {
-  uint32_t sc2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(sc2) : "h"((uint16_t)(scale | (scale << 8))));
-  const __half2 s2 = *reinterpret_cast<const __half2*>(&sc2);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint32_t word = i < 4 ? codes.x : codes.y;
-    const uint16_t byte = (uint16_t)((word >> (8 * (i & 3))) & 0xFFu);
-    uint32_t h2;
-    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u16 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-        : "=r"(h2)
-        : "h"(byte));
-    const __half2 v2 = __hmul2(*reinterpret_cast<const __half2*>(&h2), s2);
-    const float2 f = __half22float2(v2);
-    out[i] = pack_bf16x2(f.x, f.y);
-  }
-}
-
 // Converts one staged NVFP4 slice (kFp4Data code bytes, then kFp4Scales
 // scales) into the two 64-column bf16 halves the MMA reads (SWIZZLE_128B
 // image), or writes zeros when the slice's page is unmapped.
@@ -954,8 +920,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       tc_fence_after();
       const size_t part = ((size_t)(it.tail < 0 ? 0 : it.tail) * a.splits + it.split) * a.rows_part;
       const bool has = lt > 0.f;
-      float os = 1.f;  // output scale (the NVFP4 V global scale)
-      if constexpr (FP8) os = a.out_scale;
+      const float os = a.out_scale;  // output scale (the NVFP4 V global scale; else 1)
       const float inv = has ? os / lt : 0.f;
       auto store_half = [&](int half, const float* o) {
         if (!active) return;
@@ -976,8 +941,7 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
           float4* dst = reinterpret_cast<float4*>(a.part_o + (part + row) * 128 + half * 64);
 #pragma unroll
           for (int c = 0; c < 64; c += 4)
-            dst[c >> 2] = FP8 ? make_float4(o[c] * os, o[c + 1] * os, o[c + 2] * os, o[c + 3] * os)
-                              : make_float4(o[c], o[c + 1], o[c + 2], o[c + 3]);
+            dst[c >> 2] = make_float4(o[c] * os, o[c + 1] * os, o[c + 2] * os, o[c + 3] * os);
         }
       };
       // O is released (the next item's first PV may overwrite it) as soon as

@@ -55,14 +55,20 @@ size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_he
 
 /*
  * Workspace bytes for the forward's fastest route with these K/V: the size
- * above, plus, for flat MSA_FP8_E4M3 K/V on a prefill-sized call (total_q *
- * num_qo_heads >= total_k * num_kv_heads), room for a bf16 copy of K and of
- * V (2 * 256-byte-rounded total_k * num_kv_heads * head_dim * 2 bytes). Given
- * that much, the forward decodes E4M3 K/V into the copy with one HBM-bound
+ * above, plus, for MSA_FP8_E4M3 K/V on a prefill-sized call, room for a bf16
+ * copy of K and V:
+ *   flat (paged == 0; total_k = key rows): when total_q * num_qo_heads >=
+ *     total_k * num_kv_heads, 2 * 256-byte-rounded total_k * num_kv_heads *
+ *     head_dim * 2 bytes;
+ *   paged (paged != 0; total_k = max_pages, the page table's width): when
+ *     total_q * num_qo_heads >= batch * max_pages * 128 * num_kv_heads, a bf16
+ *     page pool of batch * max_pages pages for K and for V plus a renumbered
+ *     page table (each 256-byte rounded).
+ * Given that much, the forward decodes E4M3 into the copy with one HBM-bound
  * pass and runs the attention kernel on bf16 operands; given only the size
  * above, the attention kernel converts E4M3 itself (same results, slower on
- * tensor-bound calls). Equals the size above for every other case; total_k
- * is ignored when paged. Returns 0 where the size above does or total_k < 0.
+ * tensor-bound calls). Equals the size above for every other case. Returns 0
+ * where the size above does or total_k < 0.
  */
 size_t msa_sparse_attention_workspace_size_kv(int batch, int total_q, int num_qo_heads,
                                               int num_kv_heads, int head_dim, int topk,
@@ -173,8 +179,15 @@ void msa_sparse_attention_plan_free(msa_attention_plan_t* plan);
  *   k_global_scale, v_global_scale  positive, finite; the K one folds into the
  *                 softmax scale, the V one into the output;
  *   q             bf16 only; other arguments as msa_sparse_attention_fwd with
- *                 cu_seqlens_k = NULL, causal = 1 and the workspace of
- *                 msa_sparse_attention_workspace_size(..., paged = 1).
+ *                 cu_seqlens_k = NULL and causal = 1;
+ *   workspace     at least msa_sparse_attention_workspace_size(..., paged = 1)
+ *                 bytes. msa_sparse_attention_nvfp4_workspace_size adds, for
+ *                 prefill-sized calls (total_q * num_qo_heads >= batch *
+ *                 max_pages * 128 * num_kv_heads), a bf16 page pool and a
+ *                 renumbered page table: given that much, the pages the batch
+ *                 can read are decoded to bf16 once and the attention kernel
+ *                 runs on bf16 operands; otherwise it decodes NVFP4 in-kernel
+ *                 (same results).
  * Unmapped pages (page id outside [0, num_pages)) are neither read nor used.
  * Returns MSA_INVALID_ARG for a NULL or misaligned pointer, a page stride not
  * a positive multiple of 16, or a global scale that is not positive and
@@ -182,6 +195,9 @@ void msa_sparse_attention_plan_free(msa_attention_plan_t* plan);
  * msa_sparse_attention_nvfp4_prepare binds the same call into a plan that
  * msa_sparse_attention_run launches (the pages' prepare / runner interface).
  */
+size_t msa_sparse_attention_nvfp4_workspace_size(int batch, int total_q, int num_qo_heads,
+                                                 int num_kv_heads, int head_dim, int topk,
+                                                 int max_seqlen_q, int max_pages);
 msa_status_t msa_sparse_attention_nvfp4_paged(
     const void* q, msa_dtype_t q_dtype, const void* k, const void* k_scale, const void* v,
     const void* v_scale, long long page_stride_bytes, float k_global_scale,

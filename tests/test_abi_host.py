@@ -105,6 +105,29 @@ def test_workspace_size_with_kv_route(L):
             == base + 2 * copy)
 
 
+def test_paged_copy_route_sizes(L):
+    """Paged E4M3 (total_k carrying the page table width) and NVFP4 add a bf16
+    page pool of batch x max_pages pages for K and V plus the renumbered table
+    exactly on prefill-sized calls (query rows x query heads at least
+    batch x max_pages x 128 x KV heads)."""
+    import block_sparse_top_msa_gb300 as msa
+    E4M3 = 2
+    r256 = lambda x: (x + 255) // 256 * 256
+    pool = lambda b, mp, hkv: 2 * r256(b * mp * hkv * 128 * 128 * 2) + r256(b * mp * 4)
+    args = (2, 4096, 32, 4, 128, 16, 2048)
+    base = msa.msa_sparse_attention_workspace_size(*args, 1)
+    assert msa.msa_sparse_attention_workspace_size_kv(*args, 1, E4M3, 8) == base + pool(2, 8, 4)
+    assert msa.msa_sparse_attention_nvfp4_workspace_size(*args, 8) == base + pool(2, 8, 4)
+    # the boundary: 4096 x 32 = 2 x 128 x 128 x 4
+    assert msa.msa_sparse_attention_nvfp4_workspace_size(*args, 128) == base + pool(2, 128, 4)
+    assert msa.msa_sparse_attention_nvfp4_workspace_size(*args, 129) == base
+    assert msa.msa_sparse_attention_workspace_size_kv(*args, 1, 0, 8) == base  # bf16: no copy
+    dec = (128, 128, 64, 4, 128, 16, 1)
+    assert (msa.msa_sparse_attention_nvfp4_workspace_size(*dec, 1024)
+            == msa.msa_sparse_attention_workspace_size(*dec, 1))
+    assert msa.msa_sparse_attention_nvfp4_workspace_size(*args, 0) == 0
+
+
 A = 0x10000  # a 64 KiB-aligned fake device address; never dereferenced on these paths
 
 

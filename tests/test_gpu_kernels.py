@@ -384,10 +384,16 @@ def _nvfp4_inputs(g, seqused, lens_q, hq, hkv, topk, bad_page=False):
                 seqused_k=torch.tensor(seqused, dtype=torch.int32)), npg
 
 
-def _nvfp4_run(msa, dev, hkv, runner=False):
+def _nvfp4_run(msa, dev, hkv, runner=False, plain_workspace=False):
     k, ks, v, vs = msa.nvfp4_views(dev["pool"], hkv)
     kw = dict(page_table=dev["page_table"], seqused_k=dev["seqused_k"],
               k_global_scale=NVFP4_KGS, v_global_scale=NVFP4_VGS, return_softmax_lse=True)
+    if plain_workspace:  # the paged size only: NVFP4 is decoded inside the attention kernel
+        cu = dev["cu_seqlens_q"]
+        n = msa.msa_sparse_attention_workspace_size(
+            cu.numel() - 1, dev["q"].shape[0], dev["q"].shape[1], hkv, 128,
+            dev["q2k_indices"].shape[2], int((cu[1:] - cu[:-1]).max()), True)
+        kw["workspace"] = torch.empty(n, dtype=torch.uint8, device=DEV)
     if runner:
         r = msa.Nvfp4AttentionRunner(dev["q"], k, ks, v, vs, dev["q2k_indices"],
                                      dev["cu_seqlens_q"], **kw)
@@ -408,6 +414,8 @@ NVFP4_CASES = [
     ("sq4_g16_unmapped", [2000, 300, 130], [4] * 3, 32, 2, 16, True),
     ("sq3_g4", [1500, 257, 10], [3, 3, 3], 8, 2, 5, False),
     ("prefill_lq_le_lk", [700, 300], [40, 300], 8, 2, 6, True),
+    # prefill-sized: the default workspace takes the bf16 page-pool route
+    ("prefill_pool_route", [700, 300], [700, 300], 8, 2, 6, True),
 ]
 
 
@@ -425,6 +433,37 @@ def test_nvfp4_paged_parity(msa, case):
         host["q"], kf, vf, host["q2k_indices"], host["cu_seqlens_q"], causal=True,
         page_table=host["page_table"], seqused_k=host["seqused_k"], num_pages=npg)
     check_attention(out, lse, ref_out, ref_lse, label=f"nvfp4_{name}")
+
+
+def test_nvfp4_routes_agree(msa):
+    """A prefill-sized call on both routes, the bf16 page pool (default
+    workspace) and the in-kernel decode (paged workspace size only), each
+    against the oracle."""
+    g = torch.Generator().manual_seed(23)
+    host, npg = _nvfp4_inputs(g, [1100, 260, 129], [1100, 260, 129], 8, 2, 8, bad_page=True)
+    dev = to_dev(host, DEV)
+    kf, vf = oracle.nvfp4_dequant(host["pool"], 2, 128, NVFP4_KGS, NVFP4_VGS)
+    ref_out, ref_lse = oracle.sparse_attention(
+        host["q"], kf, vf, host["q2k_indices"], host["cu_seqlens_q"], causal=True,
+        page_table=host["page_table"], seqused_k=host["seqused_k"], num_pages=npg)
+    for plain in (False, True):
+        out, lse = _nvfp4_run(msa, dev, 2, plain_workspace=plain)
+        check_attention(out, lse, ref_out, ref_lse, label=f"nvfp4_route_plain{plain}")
+
+
+def test_e4m3_paged_pool_route(msa):
+    """Prefill-sized paged E4M3: the default workspace decodes the pages into
+    a bf16 pool (renumbered table, one unmapped page); the paged size keeps
+    the in-kernel conversion; both against the oracle."""
+    lens = [700, 300]
+    flat = _prefill_inputs(lens, lens, 8, 2, 5, seed=31, kv="e4m3")
+    inp = _paged(flat, lens, seed=5, bad_page=True)
+    ref_out, ref_lse = _oracle(inp)
+    out, lse = _run_prefill(msa, inp)
+    check_attention(out, lse, ref_out, ref_lse, label="e4m3_paged_pool")
+    n = msa.msa_sparse_attention_workspace_size(2, sum(lens), 8, 2, 128, 5, max(lens), True)
+    out2, lse2 = _run_prefill(msa, inp, workspace=torch.empty(n, dtype=torch.uint8, device=DEV))
+    check_attention(out2, lse2, ref_out, ref_lse, label="e4m3_paged_in_kernel")
 
 
 def test_nvfp4_runner_matches_forward(msa):

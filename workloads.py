@@ -186,6 +186,35 @@ def make_prefill(spec: PrefillSpec, seed: int, device="cpu"):
                 causal=spec.causal, softmax_scale=d ** -0.5, lengths=lens)
 
 
+def make_paged_prefill_nvfp4(spec: PrefillSpec, seed: int, device="cpu",
+                             k_global_scale=0.25, v_global_scale=0.125):
+    """A paged prefill over a planar NVFP4 page pool: each sequence's pages are
+    a random permutation of the pool; selections as make_prefill."""
+    lens = prefill_lengths(spec, seed)
+    gl = _gen(seed + 7919, "cpu")
+    pages_per = [(n + BLOCK - 1) // BLOCK for n in lens]
+    num_pages = sum(pages_per)
+    perm = torch.randperm(num_pages, generator=gl).to(torch.int32)
+    page_table = torch.zeros((len(lens), max(pages_per)), dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(pages_per):
+        page_table[b, :n] = perm[off:off + n]
+        off += n
+    g = _gen(seed, device)
+    d = spec.head_dim
+    q = randn_chunked((sum(lens), spec.num_qo_heads, d), g, device, torch.bfloat16)
+    pool = nvfp4_pool(num_pages, spec.num_kv_heads, g, device, d)
+    cu = cu_from_lengths(lens, device)
+    pos = query_positions(cu.cpu(), lens).to(device)
+    q2k = select_blocks(pos, spec.num_kv_heads, spec.topk, g, first=spec.first_prev,
+                        prev=spec.first_prev)
+    return dict(q=q, kv_pool=pool, q2k_indices=q2k, cu_seqlens_q=cu,
+                page_table=page_table.to(device),
+                seqused_k=torch.tensor(lens, dtype=torch.int32, device=device),
+                softmax_scale=d ** -0.5, lengths=lens, k_global_scale=k_global_scale,
+                v_global_scale=v_global_scale)
+
+
 # --------------------------------------------------------------------------
 # Paged decode
 # --------------------------------------------------------------------------
@@ -290,6 +319,8 @@ PAGED_DECODE = DecodeSpec("paged_decode_b128_U[8192,131072]_h64kv4_top16", 128, 
 # Global scales chosen so that the decoded K and V have about unit RMS (the
 # pool's E2M1 x block-scale values have RMS about 5), like the N(0,1) values
 # of the other workloads.
+PAGED_PREFILL_NVFP4 = PrefillSpec("nvfp4_paged_prefill_4x16384_h32kv4_top16", [16384] * 4, 32, 4,
+                                  16, first_prev=True)
 PAGED_DECODE_NVFP4 = DecodeSpec("nvfp4_paged_decode_b128_U[8192,131072]_h64kv4_top16", 128,
                                 (8192, 131072), 64, 4, 16, kv_dtype="nvfp4",
                                 k_global_scale=0.25, v_global_scale=0.125)
