@@ -70,7 +70,9 @@ struct Item {
 // Warp roles. The softmax runs in kSoftmaxWG warpgroups; with two, warps q
 // and q + 4 share TMEM lanes 32q..32q+31 and split each S row by columns
 // (0..63 and 64..127), exchanging their partial row maxima every block. The
-// E4M3 variant keeps one warpgroup: its converter warps need the registers.
+// E4M3 / NVFP4 variant keeps one warpgroup and spends the registers on six
+// converter warps (12 warps at 168 registers); its conversion is latency-
+// bound, and four converters were measured 5-7% slower.
 template <bool FP8>
 struct Roles {
   static constexpr int kSoftmaxWG = FP8 ? 1 : 2;
@@ -78,8 +80,8 @@ struct Roles {
   static constexpr int kProducerWarp = kSoftmaxWarps;              // Q and K (E4M3: K and V)
   static constexpr int kMmaWarp = kSoftmaxWarps + 1;
   static constexpr int kVProducerWarp = FP8 ? -1 : kSoftmaxWarps + 2;  // V (bf16 only)
-  static constexpr int kConvWarp0 = kSoftmaxWarps + 2;              // E4M3 converters
-  static constexpr int kConvWarps = 4;
+  static constexpr int kConvWarp0 = kSoftmaxWarps + 2;              // E4M3 / NVFP4 converters
+  static constexpr int kConvWarps = 6;
   static constexpr int kWarps = kSoftmaxWarps + 2 + (FP8 ? kConvWarps : 1);
   // Readers of the item ring (the K producer writes it): V producer (bf16),
   // the MMA issuer's two cursors, every softmax warp, every converter warp.
@@ -200,9 +202,8 @@ MSA_DEV void exp_pack_store(const float* sv, float2 sc2, float neg_m, float2& ac
 // into the two 64-column bf16 halves the MMA reads, with kThreads threads.
 template <int kThreads>
 MSA_DEV void convert_tile(const uint8_t* src, uint8_t* dst_half0, int t) {
-#pragma unroll 4
-  for (int j = 0; j < 1024 / kThreads; ++j) {
-    const int i = t + j * kThreads;
+#pragma unroll 2
+  for (int i = t; i < 1024; i += kThreads) {
     const int r = i >> 3, c = i & 7;
     const uint4 raw = *reinterpret_cast<const uint4*>(src + sw128_offset(r, c));
     uint32_t outw[8];
@@ -235,9 +236,8 @@ MSA_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar
 template <int kThreads>
 MSA_DEV void convert_fp4_tile(const uint8_t* src, bool v_order, bool valid, uint8_t* dst_half0,
                               int t) {
-#pragma unroll 4
-  for (int j = 0; j < 1024 / kThreads; ++j) {
-    const int i = t + j * kThreads;
+#pragma unroll 2
+  for (int i = t; i < 1024; i += kThreads) {
     const int r = i >> 3, c = i & 7;  // token r, elements 16c .. 16c + 15
     uint32_t outw[8];
     if (valid) {
