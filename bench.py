@@ -79,20 +79,26 @@ def barrier(world):
 # ---------------------------------------------------------------- measurement helpers
 # DRAM bytes per launch of the headline attention kernel, from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum; see the profile named below).
-# Reported only while the kernel sources still hash to the fingerprint of the
-# build that was captured; otherwise the roofline's "traffic" is null.
+# Reported only while the kernel sources' code still hashes to the fingerprint
+# of the build that was captured; otherwise the roofline's "traffic" is null.
 TRAFFIC_SOURCES = ("prefill.cu", "common.cuh", "tmem_wide.cuh", "internal.h", "tmap.h", "api.cu",
                    "union.cu", "tile_map.cuh")
-TRAFFIC_MEASURED = {"fingerprint": "bf8f1ebfb2f447b7", "bytes_per_launch": 2.425e9,
+TRAFFIC_MEASURED = {"fingerprint": "0b7b540fdebbb95c", "bytes_per_launch": 2.425e9,
                     "profile": "profiles/prefill_kernel_flat_varlen_2x32768_traffic.md"}
 
 
 def kernel_fingerprint():
+    """Hash of the kernel sources' code: comments and blank lines are left
+    out, so editing a comment keeps a capture valid and editing code does not."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in TRAFFIC_SOURCES:
-        with open(os.path.join(ROOT, "block_sparse_top_msa_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "block_sparse_top_msa_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 

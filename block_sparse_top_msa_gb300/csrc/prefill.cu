@@ -1,26 +1,33 @@
-// MSA sparse attention prefill for sm_103a ("flashinfer.msa_ops.msa_sparse_attention":
-// each query attends only the top-K KV blocks selected in q2k_indices; query
-// tokens are processed in tiles, each running one online softmax over the
-// union of the blocks its tokens selected, writing the final output directly).
+// MSA sparse attention for sm_103a, prefill and paged decode
+// ("flashinfer.msa_ops.msa_sparse_attention": each query attends only the
+// top-K KV blocks selected in q2k_indices; query tokens are processed in
+// tiles, each running one online softmax over the union of the blocks its
+// tokens selected).
 //
-// One CTA per (query tile, KV head). A tile is W = 128 / G consecutive query
-// tokens of one sequence, i.e. 128 rows (token w, query head g) = one
-// tcgen05 M=128 tile; row r lives in TMEM lane r. For each block u of the
-// tile's union list:
-//   producer warp : TMA-gathers K_u and V_u (128 tokens x 128 dims) into a
-//                   two-stage shared-memory ring (flat rows cu_k[b] + 128*id,
-//                   or page page_table[b, id]); for E4M3 K/V the bytes land in
-//                   a staging ring and converter warps upconvert them exactly
-//                   to bf16 in the MMA's swizzled layout;
-//   MMA warp      : S_u = Q K_u^T (fp32, TMEM, double-buffered), then, once
-//                   the softmax has produced P_{u-1}, O += P_{u-1} V_{u-1}
-//                   with P read from TMEM;
-//   softmax warps : thread r loads its S row, masks keys by block membership
-//                   of its token, causality (key <= Lk - Lq + i) and the
-//                   sequence end, updates the running max (rescaling O only
-//                   when the max grows by more than 2^8), writes P = 2^(s*scale*log2e - m)
-//                   as bf16 into TMEM, and at the end writes O / l and the
-//                   natural-log LSE.
+// A persistent grid (one CTA per SM) walks work items: a query tile of
+// W = 128 / G consecutive tokens of one sequence (128 rows (token w, query
+// head g) = one tcgen05 M=128 tile, row r in TMEM lane r), a KV head, and a
+// slice of the tile's union list (whole lists, except for the last round of
+// decode-sized launches, whose lists are split and merged afterwards by
+// merge_splits_kernel). Roles per CTA, for each union block u:
+//   K producer    : claims the CTA's next item from a launch-wide counter,
+//                   publishes it to the other roles, loads the item's Q tile
+//                   and TMA-gathers K_u (flat rows cu_k[b] + 128 id, or page
+//                   page_table[b, id]) into a three-deep ring;
+//   V producer    : the same for V_u (bf16 / fp16 K/V);
+//   MMA warp      : S_u = Q K_u^T (fp32, TMEM, three S buffers, QK running
+//                   two blocks ahead), then O += P_u V_u with P read from TMEM;
+//   softmax warps : two warpgroups split each S row by columns; a thread
+//                   masks its row's keys by block membership of its token,
+//                   causality (key <= Lk - Lq + i) and the sequence end,
+//                   updates the running max (rescaling O only when the max
+//                   grows by more than 2^8), writes P = 2^(s*scale*log2e - m)
+//                   into TMEM, and at the end of an item writes O / l and the
+//                   natural-log LSE (or fp32 partials of a split item).
+// E4M3 and packed NVFP4 K/V (the FP8 instance): one softmax warpgroup, and
+// the producer fills a staging ring (TMA for E4M3, bulk copies of the
+// planar page's code and scale slices for NVFP4) that six converter warps
+// decode exactly to bf16 in the MMA's swizzled layout.
 // Rows whose token did not select block u get P = 0 for it, so each row's
 // result is exactly its own blocks' softmax attention.
 #include <math.h>
