@@ -14,9 +14,12 @@ roofline    the attention kernel alone (CUDA events the library records on the
             launching stream between its own launches) against the measured
             bf16 tensor peak
 cpu_baseline  the fp64 CPU oracle on a bounded row sample of the same workload
-decode / two_stage  secondary measurements on the paged-decode workload
-            (KV GB/s vs HBM) and on the two-stage proxy -> top-k -> attention
-            pipeline, each kernel timed alone with L2 flushed between launches
+decode / decode_nvfp4 / prefill_nvfp4 / two_stage / e4m3_prefill
+            secondary measurements: the paged decode with bf16 and with packed
+            NVFP4 K/V (KV GB/s vs HBM), the paged NVFP4 prefill and the flat
+            E4M3 prefill on both of their routes (TFLOP/s), and the two-stage
+            proxy -> top-k -> attention pipeline; each timed with L2 flushed
+            between launches
 
 ``--impl reference`` times the oracle itself (host cores) on a bounded sample.
 Under torchrun with N > 1 every rank runs the same workload on its own GPU
