@@ -463,11 +463,16 @@ def bench_decode(msa, device, flush, seed=0, small=False, sqs=(1, 4), reps=7):
     return out
 
 
-def bench_decode_nvfp4(msa, device, flush, seed=0, sqs=(1, 4), reps=7):
+DECODE_NVFP4_PROFILE_SPEC = workloads.DecodeSpec(
+    "nvfp4_paged_decode_b64_U[8192,32768]_h64kv4_top16", 64, (8192, 32768), 64, 4, 16,
+    kv_dtype="nvfp4", k_global_scale=0.25, v_global_scale=0.125)
+
+
+def bench_decode_nvfp4(msa, device, flush, seed=0, sqs=(1, 4), reps=7, small=False):
     """Paged decode with packed NVFP4 K/V (planar page pool, E4M3 block scales,
     global scales): the same batch, selection and metric as the bf16 decode;
     K/V bytes are 64 code + 8 scale bytes per token and side."""
-    spec = workloads.PAGED_DECODE_NVFP4
+    spec = DECODE_NVFP4_PROFILE_SPEC if small else workloads.PAGED_DECODE_NVFP4
     out = {}
     pk = peaks()
     for sq in sqs:
@@ -783,6 +788,8 @@ def main():
                     help="profiling case: paged decode only, 64 requests, seqlen_q SQ")
     ap.add_argument("--profile-e4m3", action="store_true",
                     help="profiling case: the E4M3 K/V varlen prefill only")
+    ap.add_argument("--profile-nvfp4-small", action="store_true",
+                    help="profiling case: the NVFP4 paged decode on 64 requests, s_q 1")
     ap.add_argument("--profile-nvfp4", action="store_true",
                     help="profiling case: the packed NVFP4 paged decode only")
     ap.add_argument("--profile-two-stage", action="store_true",
@@ -806,6 +813,11 @@ def main():
         r = bench_decode(msa, device, flush, small=True, sqs=(args.profile_decode,),
                          reps=args.steps)
         print(json.dumps({"profile_decode": r}))
+        return 0
+    if args.profile_nvfp4_small:
+        flush = l2_flush_buffer(device)
+        print(json.dumps({"profile_nvfp4_small": bench_decode_nvfp4(
+            msa, device, flush, sqs=(1,), reps=args.steps, small=True)}))
         return 0
     if args.profile_nvfp4:
         flush = l2_flush_buffer(device)
