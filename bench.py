@@ -378,6 +378,21 @@ def bench_prefill(msa, args, device, world, rank):
         e2e_step(i)
     torch.cuda.synchronize(device)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # The copies alone, once each, for reading the pipelined time against.
+    s.record(s_in)
+    with torch.cuda.stream(s_in):
+        for k2, v2 in host.items():
+            sets[0][k2].copy_(v2, non_blocking=True)
+    e.record(s_in)
+    torch.cuda.synchronize(device)
+    h2d_ms = s.elapsed_time(e)
+    s.record(s_out)
+    with torch.cuda.stream(s_out):
+        out_h[0].copy_(outs[0], non_blocking=True)
+        lse_h[0].copy_(lses[0], non_blocking=True)
+    e.record(s_out)
+    torch.cuda.synchronize(device)
+    d2h_ms = s.elapsed_time(e)
     # At least 10 steps: the pipeline's fill (first copy-in) and drain (last
     # copy-out) are paid once per timed run.
     n_e2e = max(10, args.steps)
@@ -391,6 +406,7 @@ def bench_prefill(msa, args, device, world, rank):
     res["e2e"] = {"value": round(aggregate_value(flops, world, e2e_s) / 1e12, 3),
                   "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                   "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_s * 1e3, 3),
+                  "h2d_ms_alone": round(h2d_ms, 3), "d2h_ms_alone": round(d2h_ms, 3),
                   "pipelined": "copy-in, compute, copy-out on three streams, two buffer sets"}
     return res
 
