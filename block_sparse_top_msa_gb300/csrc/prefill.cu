@@ -1019,7 +1019,9 @@ cudaError_t launch_dependent(Kernel kernel, dim3 grid, dim3 block, size_t smem, 
 // lse = (M + log2 L) ln 2 (m in log2 units of the scaled logits). One warp per
 // (tail unit, row); each lane owns four of the 128 dims.
 __global__ void __launch_bounds__(256) merge_splits_kernel(const __grid_constant__ PrefillArgs a) {
-  grid_dependency_wait();  // partials of the attention kernel launched just before
+  // The union metadata read below is final before this launch may begin: the
+  // attention kernel lets it launch only after waiting for the union kernel.
+  // Only the partials need the wait, so it comes after the metadata loads.
   const int warp_global = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (warp_global >= a.tail_units * a.rows_part) return;
@@ -1038,22 +1040,28 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const __grid_constant
   const int w = row / G, gh = row - w * G;
   if (row >= a.tile_tokens * G || w >= nw) return;
   const size_t p0 = (size_t)t * a.splits * a.rows_part + row;
+  grid_dependency_wait();  // partials of the attention kernel launched just before
   float M = -INFINITY;
+#pragma unroll 4
   for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldg(a.part_ml + (p0 + (size_t)sp * a.rows_part) * 2));
   float L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
+#pragma unroll 4
     for (int sp = 0; sp < nsplit; ++sp) {
       const size_t pr = p0 + (size_t)sp * a.rows_part;
-      const float ms = __ldg(a.part_ml + pr * 2);
-      if (ms == -INFINITY) continue;
-      const float f = ex2(ms - M);
-      L += f * __ldg(a.part_ml + pr * 2 + 1);
+      const float2 ml = __ldg(reinterpret_cast<const float2*>(a.part_ml) + pr);
       const float4 ov = __ldg(reinterpret_cast<const float4*>(a.part_o + pr * 128) + lane);
-      acc.x += f * ov.x;
-      acc.y += f * ov.y;
-      acc.z += f * ov.z;
-      acc.w += f * ov.w;
+      // A split with no visible key (m = -inf) contributes nothing; its O
+      // slot is loaded with the others but not used.
+      if (ml.x != -INFINITY) {
+        const float f = ex2(ml.x - M);
+        L += f * ml.y;
+        acc.x += f * ov.x;
+        acc.y += f * ov.y;
+        acc.z += f * ov.z;
+        acc.w += f * ov.w;
+      }
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
