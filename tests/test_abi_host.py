@@ -281,3 +281,26 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(msa, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         msa.lib()
+
+
+def test_nvfp4_views_follow_the_planar_page():
+    """nvfp4_views exposes the four regions of each planar page as the strided
+    (pages, Hkv, 128, bytes) views the NVFP4 entry point documents."""
+    import block_sparse_top_msa_gb300 as msa
+    import workloads
+    hkv, npg = 3, 5
+    stride = workloads.nvfp4_page_stride(hkv)
+    assert stride == 2 * hkv * 128 * (64 + 8)
+    pool = (torch.arange(npg * stride, dtype=torch.int64) % 251).to(torch.uint8).view(npg, stride)
+    k, ks, v, vs = msa.nvfp4_views(pool, hkv)
+    assert k.shape == v.shape == (npg, hkv, 128, 64)
+    assert ks.shape == vs.shape == (npg, hkv, 128, 8)
+    for t in (k, ks, v, vs):
+        assert t.stride(0) == stride
+    data, sc = hkv * 128 * 64, hkv * 128 * 8
+    flat = pool.reshape(-1)
+    p, h, r = 4, 2, 77
+    assert int(k[p, h, r, 9]) == int(flat[p * stride + h * 8192 + r * 64 + 9])
+    assert int(ks[p, h, r, 5]) == int(flat[p * stride + data + h * 1024 + r * 8 + 5])
+    assert int(v[p, h, r, 63]) == int(flat[p * stride + data + sc + h * 8192 + r * 64 + 63])
+    assert int(vs[p, h, r, 0]) == int(flat[p * stride + 2 * data + sc + h * 1024 + r * 8])
