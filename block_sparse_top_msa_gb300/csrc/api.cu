@@ -358,8 +358,9 @@ msa_status_t build_forward(
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
   const float scale_log2 = scale * 1.4426950408889634f;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  // The bf16-copy route needs its two copies after the layout's regions; with
-  // a smaller workspace the kernel converts E4M3 itself.
+  // E4M3 on a prefill-sized call: the flat copy or the paged page pool goes
+  // after the layout's regions when the workspace holds it; with a smaller
+  // workspace the attention kernel converts E4M3 itself.
   const size_t copy = kv_copy_bytes(total_k, num_kv_heads);
   if (kv_decode_route(kv_dtype, paged, total_q, num_qo_heads, total_k, num_kv_heads) &&
       workspace_bytes >= need + 2 * copy) {
