@@ -683,8 +683,15 @@ def bench_two_stage(msa, device, flush, seed=0):
     G = spec.num_qo_heads // spec.num_kv_heads
     cnt = visible_counts(q2k, inp["cu_seqlens_q"], spec.seqlens)
     aflops = 4.0 * D * G * float(cnt.sum())
+    W = msa.msa_union_tile_tokens(spec.num_qo_heads, spec.num_kv_heads)
+    ulen = msa.msa_build_union(q2k, inp["cu_seqlens_q"], inp["cu_seqlens_k"], causal=True,
+                               tile_tokens=W)[0]
+    flops_exec = float(ulen.sum().item()) * 4.0 * D * 128 * 128
     res["attention"] = {"tflops": round(aflops / t_attn / 1e12, 2), "ms": round(t_attn * 1e3, 3),
-                        "frac_of_bf16_peak": round(aflops / t_attn / 1e12 / pk["bf16"], 4)}
+                        "frac_of_bf16_peak": round(aflops / t_attn / 1e12 / pk["bf16"], 4),
+                        "executed_mma_tflops": round(flops_exec / t_attn / 1e12, 2),
+                        "work_efficiency": round(aflops / flops_exec, 4),
+                        "union_blocks_per_tile": round(float(ulen[ulen > 0].float().mean().item()), 2)}
     res["pipeline_ms"] = round((t_proxy + t_topk + t_attn) * 1e3, 3)
     return res
 
