@@ -528,6 +528,19 @@ def test_decode_f16(msa, sq):
     check_attention(out, lse, ref_out, ref_lse, label=f"f16_decode_sq{sq}")
 
 
+@pytest.mark.parametrize("sq", [1, 4])
+def test_decode_e4m3(msa, sq):
+    """Paged E4M3 K/V at decode size: the converter-warp instance with the
+    union split over work items and the merge of the partials."""
+    seqused = [4000, 700, 129, 2600]
+    inp = _decode_inputs(torch.Generator().manual_seed(60 + sq), seqused, sq, 32, 2, 16)
+    inp["k"] = inp["k"].float().clamp(-448, 448).to(torch.float8_e4m3fn)
+    inp["v"] = inp["v"].float().clamp(-448, 448).to(torch.float8_e4m3fn)
+    out, lse = _run_prefill(msa, inp, max_seqlen_q=sq)
+    ref_out, ref_lse = _oracle(inp)
+    check_attention(out, lse, ref_out, ref_lse, label=f"e4m3_decode_sq{sq}")
+
+
 def test_prepared_runner_matches_forward(msa):
     """A prepared forward gives the plain forward's bits, refilled inputs give
     fresh results, and its run captures into a CUDA graph."""
