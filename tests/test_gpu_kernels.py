@@ -466,6 +466,45 @@ def test_e4m3_paged_pool_route(msa):
     check_attention(out2, lse2, ref_out, ref_lse, label="e4m3_paged_in_kernel")
 
 
+def test_nvfp4_pool_route_graph_replay(msa):
+    """The prepared NVFP4 forward on its page-pool route (page decode, union
+    and attention kernels) captured once into a CUDA graph; each replay reads
+    the pool and queries refilled in place."""
+    g = torch.Generator().manual_seed(71)
+    seqused = [900, 300]
+    host, npg = _nvfp4_inputs(g, seqused, seqused, 8, 2, 6)
+    dev = to_dev(host, DEV)
+    k, ks, v, vs = msa.nvfp4_views(dev["pool"], 2)
+    r = msa.Nvfp4AttentionRunner(dev["q"], k, ks, v, vs, dev["q2k_indices"], dev["cu_seqlens_q"],
+                                 page_table=dev["page_table"], seqused_k=dev["seqused_k"],
+                                 k_global_scale=NVFP4_KGS, v_global_scale=NVFP4_VGS,
+                                 return_softmax_lse=True)
+    r.run()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            r.run(stream=stream)
+    torch.cuda.synchronize()
+    for trial in range(2):
+        gt = torch.Generator().manual_seed(500 + trial)
+        new_pool = workloads.nvfp4_pool(npg, 2, gt, "cpu")
+        new_q = torch.randn(host["q"].shape, generator=gt).to(torch.bfloat16)
+        dev["pool"].copy_(new_pool)
+        dev["q"].copy_(new_q)
+        graph.replay()
+        torch.cuda.synchronize()
+        fault_clear(msa)
+        kf, vf = oracle.nvfp4_dequant(new_pool, 2, 128, NVFP4_KGS, NVFP4_VGS)
+        ref_out, ref_lse = oracle.sparse_attention(
+            new_q, kf, vf, host["q2k_indices"], host["cu_seqlens_q"], causal=True,
+            page_table=host["page_table"], seqused_k=host["seqused_k"], num_pages=npg)
+        check_attention(r.out, r.lse, ref_out, ref_lse, label=f"nvfp4_graph_{trial}")
+    r.close()
+
+
 def test_nvfp4_runner_matches_forward(msa):
     """The prepared NVFP4 forward (prepare once, run) gives the direct call's bits."""
     g = torch.Generator().manual_seed(5)
