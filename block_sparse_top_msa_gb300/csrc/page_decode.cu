@@ -7,9 +7,9 @@
 // kernel then streams bf16 tiles, which on tensor-bound calls beats
 // converting every block visit inside the attention kernel.
 //
-// One CTA per (request, block): K then V of every KV head, 16 elements
-// (16 bytes of E4M3, or 8 bytes of E2M1 pairs and their block scale) per
-// step. NVFP4 values are exact in bf16 (see fp4x16_to_bf16); the global
+// One CTA per (request, block), a 1-D grid of batch * max_pages CTAs: K then
+// V of every KV head, 16 elements (16 bytes of E4M3, or 8 bytes of E2M1 pairs
+// and their block scale) per step. NVFP4 values are exact in bf16 (see fp4x16_to_bf16); the global
 // scales are applied by the attention kernel as on the in-kernel route.
 #include "common.cuh"
 #include "internal.h"
@@ -20,8 +20,9 @@ namespace {
 constexpr int kPageThreads = 256;
 
 __global__ void __launch_bounds__(kPageThreads) pages_to_bf16_kernel(const PageDecodeArgs a) {
-  const int b = blockIdx.y, t = blockIdx.x;
-  const size_t slot = (size_t)b * a.max_pages + t;
+  const size_t slot = blockIdx.x;  // request b's block t: slot b * max_pages + t
+  const int b = (int)(slot / (size_t)a.max_pages);
+  const int t = (int)(slot - (size_t)b * a.max_pages);
   int nblk = (a.seqused_k[b] + kBlk - 1) / kBlk;
   if (nblk > a.max_pages) nblk = a.max_pages;
   const int p = t < nblk ? a.page_table[slot] : -1;
@@ -59,7 +60,9 @@ __global__ void __launch_bounds__(kPageThreads) pages_to_bf16_kernel(const PageD
 
 cudaError_t launch_page_decode(const PageDecodeArgs& a, cudaStream_t s) {
   if (a.mode == 0 || a.batch <= 0 || a.max_pages <= 0) return cudaSuccess;
-  pages_to_bf16_kernel<<<dim3((unsigned)a.max_pages, (unsigned)a.batch), kPageThreads, 0, s>>>(a);
+  const unsigned long long slots = (unsigned long long)a.batch * (unsigned long long)a.max_pages;
+  if (slots > 0x7fffffffull) return cudaErrorInvalidConfiguration;  // one CTA per slot
+  pages_to_bf16_kernel<<<(unsigned)slots, kPageThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
