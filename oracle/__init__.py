@@ -43,6 +43,7 @@ def _load():
             C.POINTER(C.c_uint32)]
         _lib.oracle_e4m3_decode.argtypes = [C.POINTER(C.c_uint8), C.c_longlong, f64p]
         _lib.oracle_bf16_decode.argtypes = [C.POINTER(C.c_uint16), C.c_longlong, f64p]
+        _lib.oracle_fp16_decode.argtypes = [C.POINTER(C.c_uint16), C.c_longlong, f64p]
         _lib.oracle_e2m1_decode.argtypes = [C.POINTER(C.c_uint8), C.c_longlong, f64p]
         _lib.oracle_nvfp4_dequant.argtypes = [
             C.POINTER(C.c_uint8), C.c_longlong, ci, ci, ci, C.c_double, C.c_double, f64p, f64p]
@@ -260,6 +261,15 @@ def bf16_decode(bits):
     a = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16))
     out = np.zeros(a.shape, dtype=np.float64)
     lib.oracle_bf16_decode(_ptr(a, C.c_uint16), a.size, _ptr(out, C.c_double))
+    return out
+
+
+def fp16_decode(bits):
+    """Values of IEEE binary16 bit patterns, decoded from the bits in fp64."""
+    lib = _load()
+    a = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16))
+    out = np.zeros(a.shape, dtype=np.float64)
+    lib.oracle_fp16_decode(_ptr(a, C.c_uint16), a.size, _ptr(out, C.c_double))
     return out
 
 

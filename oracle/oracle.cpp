@@ -185,6 +185,12 @@ void oracle_bf16_decode(const uint16_t* bits, long long n, double* out) {
   for (long long i = 0; i < n; ++i) out[i] = bf16_value(bits[i]);
 }
 
+// Decode n IEEE binary16 bit patterns to fp64 (the fp16 q / K / V of the
+// attention page's Parameters).
+void oracle_fp16_decode(const uint16_t* bits, long long n, double* out) {
+  for (long long i = 0; i < n; ++i) out[i] = fp16_value(bits[i]);
+}
+
 // Decode n E2M1 codes (low nibble of each byte) to fp64.
 void oracle_e2m1_decode(const uint8_t* codes, long long n, double* out) {
   for (long long i = 0; i < n; ++i) out[i] = e2m1_value(codes[i] & 15);

@@ -277,6 +277,49 @@ def test_bf16_decode_matches_torch():
     np.testing.assert_array_equal(got[~nan], ref[~nan])
 
 
+def test_fp16_decode_all_codes():
+    """All 65536 binary16 patterns against torch's float16 -> float64 cast, plus
+    hand-known codes (subnormal scale 2^-24, smallest normal 2^-14, bias 15,
+    largest finite 65504, infinities, -0 and the NaN patterns)."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle.fp16_decode(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.float16).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    # NaN: exponent field 31 with a non-zero mantissa, either sign.
+    exp_field, mant = (bits >> 10) & 31, bits & 1023
+    assert np.array_equal(nan, (exp_field == 31) & (mant != 0))
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    assert got[0x0001] == 2.0 ** -24 and got[0x03FF] == 1023 * 2.0 ** -24
+    assert got[0x0400] == 2.0 ** -14 and got[0x3C00] == 1.0 and got[0x3555] == 1365 / 4096
+    assert got[0x7BFF] == 65504.0 and got[0xC000] == -2.0
+    assert got[0x7C00] == math.inf and got[0xFC00] == -math.inf
+    assert got[0x8000] == 0.0 and math.copysign(1, got[0x8000]) < 0
+
+
+def test_fp16_attention_equals_bf16_on_shared_values():
+    """fp16 q / K / V give bit-identical oracle results to bf16 inputs holding
+    the same values (k/16 with |k| < 256: exact in both formats)."""
+    g = torch.Generator().manual_seed(9)
+    L, d = 300, 128
+
+    def vals(*shape):
+        return (torch.randint(-255, 256, shape, generator=g).double() / 16.0)
+
+    q, k, v = vals(L, 4, d) * 0.25, vals(L, 2, d) * 0.25, vals(L, 2, d)
+    cu = workloads.cu_from_lengths([L])
+    q2k = workloads.select_blocks(workloads.query_positions(cu, [L]), 2, 2, g)
+    for t in (q, k, v):
+        assert torch.equal(t.to(torch.float16).double(), t)
+        assert torch.equal(t.to(torch.bfloat16).double(), t)
+    oh, lh = oracle.sparse_attention(q.half(), k.half(), v.half(), q2k, cu, cu, causal=True)
+    ob, lb = oracle.sparse_attention(q.bfloat16(), k.bfloat16(), v.bfloat16(), q2k, cu, cu,
+                                     causal=True)
+    np.testing.assert_array_equal(oh, ob)
+    np.testing.assert_array_equal(lh, lb)
+    assert np.isfinite(lh).all()
+
+
 def test_e4m3_attention_uses_decoded_values():
     """An E4M3 K/V run equals the bf16 run on the same (exactly representable) values."""
     g = torch.Generator().manual_seed(8)
