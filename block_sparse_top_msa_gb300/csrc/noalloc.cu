@@ -62,9 +62,12 @@ extern "C" msa_status_t msa_sparse_decode_noalloc(
   const size_t need = msa_sparse_attention_workspace_size(
       batch, total_q, num_qo_heads, num_kv_heads, head_dim, topk, max_seqlen_q, 1);
   if (need > kNoAllocScratchBytes) return MSA_WORKSPACE_TOO_SMALL;
+  // The array is passed whenever the sizes are valid (need > 0), also for an
+  // empty call (total_q == 0), which the forward accepts and returns MSA_OK for
+  // without launching anything.
   void* ws = nullptr;
   size_t ws_bytes = 0;
-  if (need > 0 && total_q > 0) {
+  if (need > 0) {
     ws = scratch_on_current_device();
     if (ws == nullptr) return MSA_CUDA_ERROR;
     ws_bytes = kNoAllocScratchBytes;
