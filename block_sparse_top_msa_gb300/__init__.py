@@ -7,9 +7,13 @@ all computation happens in the library's CUDA kernels. There is no fallback:
 if the library has not been built, every call raises.
 
 Convenience defaults that need information the C ABI takes explicitly
-(``max_seqlen_q``, ``max_k_tiles``) are derived here from ``cu_seqlens``,
-which costs one device-to-host copy; pass them to avoid it. Output and
-workspace buffers are allocated with torch when not supplied.
+(``max_seqlen_q``, ``max_k_tiles``) are derived here from ``cu_seqlens`` /
+``seqused_k`` when omitted. That derivation READS THE DEVICE: a
+device-to-host copy that synchronises the host with the GPU and launches
+two small torch kernels on every such call. Code that must not synchronise
+(CUDA-graph capture, pipelined serving loops) passes them explicitly; the C
+ABI itself never synchronises. Output and workspace buffers are allocated
+with torch when not supplied.
 """
 from __future__ import annotations
 
@@ -87,6 +91,13 @@ def lib():
             vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
         L.msa_union_tile_tokens.restype = i32
         L.msa_union_tile_tokens.argtypes = [i32, i32]
+        L.msa_build_union_block_members.restype = i32
+        L.msa_build_union_block_members.argtypes = [
+            vp, i32, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
+        L.msa_prefill_tile_tokens.restype = i32
+        L.msa_prefill_tile_tokens.argtypes = [i32] * 7
+        L.msa_set_prefill_route.restype = i32
+        L.msa_set_prefill_route.argtypes = [i32]
         L.msa_sparse_decode_noalloc.restype = i32
         L.msa_sparse_decode_noalloc.argtypes = [
             vp, vp, vp, vp, i32, vp, vp, i32, i32, vp, i32, i32, i32, i32, i32, i32, i32, f32,
@@ -152,6 +163,22 @@ def msa_union_tile_tokens(num_qo_heads: int, num_kv_heads: int) -> int:
     return int(lib().msa_union_tile_tokens(num_qo_heads, num_kv_heads))
 
 
+def msa_prefill_tile_tokens(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q,
+                            kv_dtype=MSA_BF16) -> int:
+    """Tokens per query tile of the attention kernel the forward picks; see
+    include/msa.h. ``kv_dtype`` is a torch dtype or an MSA_* code."""
+    code = kv_dtype if isinstance(kv_dtype, int) else _dtype_code(torch.empty(0, dtype=kv_dtype))
+    return int(lib().msa_prefill_tile_tokens(batch, total_q, num_qo_heads, num_kv_heads, topk,
+                                             max_seqlen_q, code))
+
+
+def msa_set_prefill_route(route: int) -> None:
+    """0: pick the attention kernel by shape (default); 1: always the
+    union-tile kernel; 2: the swapped-orientation kernel wherever it applies.
+    Process-wide (include/msa.h)."""
+    _check("msa_set_prefill_route", lib().msa_set_prefill_route(int(route)))
+
+
 def msa_sparse_attention_workspace_size(batch, total_q, num_qo_heads, num_kv_heads, head_dim,
                                         topk, max_seqlen_q, paged) -> int:
     return int(lib().msa_sparse_attention_workspace_size(
@@ -179,7 +206,9 @@ def msa_sparse_attention_fwd(q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k=No
                              workspace=None, stream=None):
     """Sparse attention forward; see ``msa_sparse_attention_fwd`` in include/msa.h.
 
-    Returns ``out`` or ``(out, lse)``.
+    Returns ``out`` or ``(out, lse)``. With ``max_seqlen_q=None`` the longest
+    query run is read back from ``cu_seqlens_q`` on the device, which
+    synchronises the host; pass it to keep the call asynchronous.
     """
     L = lib()
     args, out, lse, workspace = _forward_args(
@@ -438,6 +467,34 @@ def msa_build_union(q2k_indices, cu_seqlens_q, cu_seqlens_k=None, *, seqused_k=N
     return ulen, ublk, mem, info
 
 
+def msa_build_union_block_members(q2k_indices, cu_seqlens_q, cu_seqlens_k=None, *,
+                                  seqused_k=None, max_pages=0, causal=True, tile_tokens=32,
+                                  max_tiles=None, stream=None):
+    """msa_build_union plus the per-union-block member-token masks
+    (tile_tokens <= 32); returns (union_len, union_blocks, member,
+    block_members, tile_info)."""
+    L = lib()
+    _cuda_contig("q2k_indices", q2k_indices, torch.int32)
+    hkv, total_q, topk = q2k_indices.shape
+    batch = cu_seqlens_q.shape[0] - 1
+    if max_tiles is None:
+        max_tiles = (total_q + tile_tokens - 1) // tile_tokens + batch
+    cap = tile_tokens * topk
+    words = (cap + 31) // 32
+    dev = q2k_indices.device
+    ulen = torch.empty((hkv, max_tiles), dtype=torch.int32, device=dev)
+    ublk = torch.empty((hkv, max_tiles, cap), dtype=torch.int32, device=dev)
+    mem = torch.empty((hkv, max_tiles, tile_tokens, words), dtype=torch.int32, device=dev)
+    bmem = torch.empty((hkv, max_tiles, cap), dtype=torch.int32, device=dev)
+    info = torch.empty((max_tiles, 2), dtype=torch.int32, device=dev)
+    st = L.msa_build_union_block_members(
+        _p(q2k_indices), topk, _p(cu_seqlens_q), _p(cu_seqlens_k), _p(seqused_k),
+        int(max_pages), batch, total_q, hkv, int(bool(causal)), int(tile_tokens), int(max_tiles),
+        _p(ulen), _p(ublk), _p(mem), _p(bmem), _p(info), _stream(stream))
+    _check("msa_build_union_block_members", st)
+    return ulen, ublk, mem, bmem, info
+
+
 def msa_read_device_fault(stream=None) -> int:
     """Synchronise the stream, return and clear the library's device fault word."""
     v = C.c_uint(0)
@@ -470,9 +527,17 @@ def msa_sparse_decode_noalloc(q, k, v, q2k_indices, cu_seqlens_q, page_table, se
     _cuda_contig("cu_seqlens_q", cu_seqlens_q, torch.int32)
     _cuda_contig("page_table", page_table, torch.int32)
     _cuda_contig("seqused_k", seqused_k, torch.int32)
+    if k.dim() != 4 or tuple(k.shape[2:]) != (128, 128) or k.shape != v.shape:
+        raise ValueError("k and v must be paged pools of shape (num_pages, Hkv, 128, 128)")
     total_q, hq, d = q.shape
     if out is None:
         out = torch.empty_like(q)
+    _cuda_contig("out", out, torch.bfloat16)
+    if tuple(out.shape) != tuple(q.shape):
+        raise ValueError("out must have q's shape")
+    _cuda_contig("lse", lse, torch.float32)
+    if lse is not None and tuple(lse.shape) != (total_q, hq):
+        raise ValueError("lse must have shape (total_q, num_qo_heads)")
     st = L.msa_sparse_decode_noalloc(
         _p(q), _p(k), _p(v), _p(q2k_indices), q2k_indices.shape[2], _p(cu_seqlens_q),
         _p(page_table), page_table.shape[1], k.shape[0], _p(seqused_k),

@@ -134,6 +134,60 @@ PrefillLayout prefill_layout(int batch, int total_q, int hq, int hkv, int topk, 
   return L;
 }
 
+// Layout of the swapped-orientation prefill kernel: query tiles of W tokens
+// with W * G <= 256 rows (W <= 32, so a tile's member tokens fit one 32-bit
+// mask per union block), no splits, and the per-block member masks.
+struct SwappedLayout {
+  bool usable;  // G a multiple of 8 and at most 64
+  int W, max_tiles, cap, words, num_items;
+  size_t off_info, off_len, off_blocks, off_member, off_bmem, off_counter, total;
+};
+
+SwappedLayout swapped_layout(int batch, int total_q, int hq, int hkv, int topk,
+                             int max_seqlen_q) {
+  SwappedLayout L{};
+  const int G = hkv > 0 ? hq / hkv : 0;
+  L.usable = G >= 8 && G <= 64 && G % 8 == 0;
+  if (!L.usable) return L;
+  L.W = 256 / G < 32 ? 256 / G : 32;
+  const int sq = max_seqlen_q < 1 ? 1 : max_seqlen_q;
+  if (sq < L.W) L.W = sq;
+  long long mt = ((long long)total_q + L.W - 1) / L.W + batch;
+  if (total_q > 0 && mt > total_q) mt = total_q;
+  if (L.W >= sq && mt > batch) mt = batch;
+  if (mt < 1) mt = 1;
+  L.max_tiles = (int)mt;
+  L.cap = L.W * topk;
+  L.words = (L.cap + 31) / 32;
+  const size_t units = (size_t)hkv * L.max_tiles;
+  L.num_items = (int)units;
+  size_t off = 0;
+  L.off_info = off;
+  off += up256((size_t)L.max_tiles * 2 * sizeof(int32_t));
+  L.off_len = off;
+  off += up256(units * sizeof(int32_t));
+  L.off_blocks = off;
+  off += up256(units * L.cap * sizeof(int32_t));
+  L.off_member = off;
+  off += up256(units * L.W * L.words * sizeof(uint32_t));
+  L.off_bmem = off;
+  off += up256(units * L.cap * sizeof(uint32_t));
+  L.off_counter = off;
+  off += 256;
+  L.total = off;
+  return L;
+}
+
+// Forward route: 0 chooses by measured speed (the union-tile kernel, for
+// now, on every workload measured), 1 always the union-tile kernel, 2 the
+// swapped kernel wherever it applies (msa_set_prefill_route).
+int g_route = 0;
+
+bool use_swapped(const SwappedLayout& S, int esize, int max_seqlen_q) {
+  (void)max_seqlen_q;
+  return S.usable && esize == 2 && g_route == 2;
+}
+
 // Flat E4M3 K/V on a prefill-sized call (at least as many query rows x query
 // heads as key rows x KV heads) is decoded to bf16 once, into the workspace,
 // and attended with the bf16 kernel: the attention kernel is tensor-bound
@@ -269,7 +323,11 @@ size_t msa_sparse_attention_workspace_size(int batch, int total_q, int num_qo_he
       num_qo_heads / num_kv_heads > 128)
     return 0;
   (void)paged;
-  return prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q).total;
+  const size_t a =
+      prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q).total;
+  const SwappedLayout S =
+      swapped_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q);
+  return S.usable && S.total > a ? S.total : a;
 }
 
 size_t msa_sparse_attention_workspace_size_kv(int batch, int total_q, int num_qo_heads,
@@ -312,7 +370,92 @@ struct ForwardPlan {
   PageDecodeArgs pd{};  // mode > 0: paged E4M3 / NVFP4 pages decoded to a bf16 pool first
   UnionArgs u{};
   PrefillArgs a{};
+  bool swapped = false;  // the swapped-orientation prefill kernel, else the union-tile kernel
 };
+
+// The swapped-kernel part of a forward plan (arguments already checked).
+msa_status_t build_swapped(const void* q, msa_dtype_t q_dtype, const void* k, const void* v,
+                           const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+                           const int32_t* cu_seqlens_k, const int32_t* page_table, int max_pages,
+                           int num_pages, const int32_t* seqused_k, int batch, int total_q,
+                           int total_k, int num_qo_heads, int num_kv_heads, int causal,
+                           float scale_log2, void* out, float* lse, uint8_t* ws,
+                           const SwappedLayout& S, unsigned* fault, ForwardPlan* plan) {
+  const bool paged = page_table != nullptr;
+  const int G = num_qo_heads / num_kv_heads;
+  plan->swapped = true;
+  UnionArgs& u = plan->u;
+  u.q2k = q2k_indices;
+  u.topk = topk;
+  u.cu_q = cu_seqlens_q;
+  u.cu_k = cu_seqlens_k;
+  u.seqused_k = seqused_k;
+  u.max_pages = max_pages;
+  u.batch = batch;
+  u.total_q = total_q;
+  u.num_kv_heads = num_kv_heads;
+  u.causal = causal ? 1 : 0;
+  u.tile_tokens = S.W;
+  u.max_tiles = S.max_tiles;
+  u.cap = S.cap;
+  u.words = S.words;
+  u.union_len = reinterpret_cast<int32_t*>(ws + S.off_len);
+  u.union_blocks = reinterpret_cast<int32_t*>(ws + S.off_blocks);
+  u.member = reinterpret_cast<uint32_t*>(ws + S.off_member);
+  u.block_members = reinterpret_cast<uint32_t*>(ws + S.off_bmem);
+  u.tile_info = reinterpret_cast<int32_t*>(ws + S.off_info);
+  u.item_counter = reinterpret_cast<int32_t*>(ws + S.off_counter);
+  PrefillArgs& a = plan->a;
+  a.fault = fault;
+  bool ok = map_rows(&a.tmap_q, q, 2, num_qo_heads, total_q, (uint32_t)G, (uint32_t)S.W) &&
+            map_rows(&a.tmap_q1, q, 2, num_qo_heads, total_q, (uint32_t)G, 1u);
+  if (paged) {
+    ok = ok && map_pages(&a.tmap_k, k, 2, num_kv_heads, num_pages) &&
+         map_pages(&a.tmap_v, v, 2, num_kv_heads, num_pages);
+  } else {
+    ok = ok && map_rows(&a.tmap_k, k, 2, num_kv_heads, total_k, 1, 128) &&
+         map_rows(&a.tmap_v, v, 2, num_kv_heads, total_k, 1, 128);
+  }
+  if (!ok) return MSA_CUDA_ERROR;
+  a.paged = paged ? 1 : 0;
+  a.kv_fp8 = 0;
+  a.kv_fp4 = 0;
+  a.out_scale = 1.f;
+  a.f16 = q_dtype == MSA_FP16 ? 1 : 0;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.page_table = page_table;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.seqused_k = seqused_k;
+  a.batch = batch;
+  a.total_q = total_q;
+  a.num_qo_heads = num_qo_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.causal = causal ? 1 : 0;
+  a.scale_log2 = scale_log2;
+  a.tile_tokens = S.W;
+  a.max_tiles = S.max_tiles;
+  a.cap = S.cap;
+  a.words = S.words;
+  a.union_len = u.union_len;
+  a.union_blocks = u.union_blocks;
+  a.member = u.member;
+  a.block_members = u.block_members;
+  a.tile_info = u.tile_info;
+  a.out = out;
+  a.lse = lse;
+  a.whole_units = S.num_items;
+  a.tail_units = 0;
+  a.splits = 1;
+  a.pps = S.cap;
+  a.rows_part = 0;
+  a.num_items = S.num_items;
+  a.part_o = nullptr;
+  a.part_ml = nullptr;
+  a.item_counter = u.item_counter;
+  return MSA_OK;
+}
 
 msa_status_t build_forward(
     const void* q, msa_dtype_t q_dtype, const void* k, const void* v, msa_dtype_t kv_dtype,
@@ -391,6 +534,13 @@ msa_status_t build_forward(
   }
   const int esize = kv_dtype == MSA_FP8_E4M3 ? 1 : 2;
 
+  const SwappedLayout S =
+      swapped_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q);
+  if (use_swapped(S, esize, max_seqlen_q))
+    return build_swapped(q, q_dtype, k, v, q2k_indices, topk, cu_seqlens_q, cu_seqlens_k,
+                         page_table, max_pages, num_pages, seqused_k, batch, total_q, total_k,
+                         num_qo_heads, num_kv_heads, causal, scale_log2, out, lse, ws, S, fault,
+                         plan);
   const PrefillLayout L =
       prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q);
   UnionArgs& u = plan->u;
@@ -543,7 +693,7 @@ msa_status_t launch_forward(const ForwardPlan& p, cudaStream_t stream) {
   e = launch_build_union(p.u, stream);
   if (e != cudaSuccess) return MSA_CUDA_ERROR;
   mark(1, stream);
-  e = launch_prefill(p.a, stream);
+  e = p.swapped ? launch_prefill_swapped(p.a, stream) : launch_prefill(p.a, stream);
   mark(2, stream);
   return from_cuda(e);
 }
@@ -771,6 +921,62 @@ msa_status_t msa_build_union(const int32_t* q2k_indices, int topk, const int32_t
   u.member = member;
   u.tile_info = tile_info;
   return from_cuda(launch_build_union(u, stream));
+}
+
+msa_status_t msa_build_union_block_members(
+    const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, const int32_t* seqused_k, int max_pages, int batch, int total_q,
+    int num_kv_heads, int causal, int tile_tokens, int max_tiles, int32_t* union_len,
+    int32_t* union_blocks, uint32_t* member, uint32_t* block_members, int32_t* tile_info,
+    cudaStream_t stream) {
+  if (block_members == nullptr || tile_tokens > 32) return MSA_INVALID_ARG;
+  if (q2k_indices == nullptr || cu_seqlens_q == nullptr || union_len == nullptr ||
+      union_blocks == nullptr || member == nullptr)
+    return MSA_INVALID_ARG;
+  if ((cu_seqlens_k == nullptr) == (seqused_k == nullptr)) return MSA_INVALID_ARG;
+  if (seqused_k != nullptr && max_pages < 1) return MSA_INVALID_ARG;
+  if (batch < 1 || total_q < 0 || num_kv_heads < 1 || max_tiles < 0) return MSA_INVALID_ARG;
+  if (tile_tokens < 1) return MSA_INVALID_ARG;
+  if (topk < 1 || topk > kMaxTopk) return MSA_UNSUPPORTED;
+  if (max_tiles == 0) return MSA_OK;
+  UnionArgs u{};
+  u.q2k = q2k_indices;
+  u.topk = topk;
+  u.cu_q = cu_seqlens_q;
+  u.cu_k = cu_seqlens_k;
+  u.seqused_k = seqused_k;
+  u.max_pages = max_pages;
+  u.batch = batch;
+  u.total_q = total_q;
+  u.num_kv_heads = num_kv_heads;
+  u.causal = causal ? 1 : 0;
+  u.tile_tokens = tile_tokens;
+  u.max_tiles = max_tiles;
+  u.cap = tile_tokens * topk;
+  u.words = (u.cap + 31) / 32;
+  u.union_len = union_len;
+  u.union_blocks = union_blocks;
+  u.member = member;
+  u.block_members = block_members;
+  u.tile_info = tile_info;
+  return from_cuda(launch_build_union(u, stream));
+}
+
+msa_status_t msa_set_prefill_route(int route) {
+  if (route < 0 || route > 2) return MSA_INVALID_ARG;
+  g_route = route;
+  return MSA_OK;
+}
+
+int msa_prefill_tile_tokens(int batch, int total_q, int num_qo_heads, int num_kv_heads,
+                            int topk, int max_seqlen_q, msa_dtype_t kv_dtype) {
+  if (batch < 1 || num_qo_heads < 1 || num_kv_heads < 1 || num_qo_heads % num_kv_heads != 0 ||
+      topk < 1 || topk > kMaxTopk)
+    return 0;
+  const SwappedLayout S =
+      swapped_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q);
+  if (use_swapped(S, kv_dtype == MSA_FP8_E4M3 ? 1 : 2, max_seqlen_q)) return S.W;
+  return prefill_layout(batch, total_q, num_qo_heads, num_kv_heads, topk, max_seqlen_q).W;
 }
 
 msa_status_t msa_set_timing_events(void* const* events, int count) {

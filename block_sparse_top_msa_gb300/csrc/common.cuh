@@ -91,6 +91,37 @@ MSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* fault, unsigned
   return mbar_wait_for(bar, parity, fault, code, kWaitLimitNs, abort);
 }
 
+// try_wait with a suspend-time hint: the thread is suspended by the hardware
+// until the phase completes or `hint_ns` elapses, so a waiting warp takes no
+// issue slots from the warps doing the work.
+MSA_DEV bool mbar_test_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait whose polls sleep (up to 100 us each) instead of spinning; the
+// same 2 s limit, abort flag and fault report.
+MSA_DEV bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, unsigned* fault, unsigned code,
+                             volatile int* abort = nullptr) {
+  if (mbar_test(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_test_hint(bar, parity, 100000u)) return true;
+    if (abort != nullptr && *abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      if (fault) atomicOr(fault, code);
+      if (abort) *abort = 1;
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 MSA_DEV void tma_prefetch_desc(const void* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
@@ -233,6 +264,34 @@ MSA_DEV void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
       "r"(r[15])
       : "memory");
+}
+
+// 32 lanes x 32 bits x 8 columns load / store without the completion wait
+// (several may be issued, then one tmem_wait_ld / tmem_wait_st).
+MSA_DEV void tmem_ld8_nowait(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+}
+MSA_DEV void tmem_st8_nowait(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+MSA_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+MSA_DEV void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 32 bits x 8 columns, waited.
+MSA_DEV void tmem_ld8(uint32_t taddr, float* v) {
+  uint32_t r[8];
+  tmem_ld8_nowait(taddr, r);
+  tmem_wait_ld();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 MSA_DEV uint32_t pack_bf16x2(float lo, float hi) {

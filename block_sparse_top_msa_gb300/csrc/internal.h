@@ -32,6 +32,10 @@ struct UnionArgs {
   uint32_t* member;
   int32_t* tile_info;  // may be NULL
   int32_t* item_counter;  // may be NULL: set to 0 (the attention kernel's work counter)
+  // May be NULL (only for tile_tokens <= 32): per union position, a mask of
+  // the tile's tokens that selected it (bit w = token w of the tile), i.e.
+  // the membership bits transposed; (num_kv_heads, max_tiles, cap) uint32.
+  uint32_t* block_members;
 };
 cudaError_t launch_build_union(const UnionArgs& a, cudaStream_t s);
 
@@ -103,8 +107,16 @@ struct PrefillArgs {
   float* part_o;        // (tail_units*splits, rows_part, 128)
   float* part_ml;       // (tail_units*splits, rows_part, 2)
   int* item_counter;    // items handed out beyond the first round; 0 at launch
+  // Swapped-orientation prefill kernel only: per union position, the mask of
+  // the tile's tokens that selected it (bit w = token w), and a q map whose
+  // box is one token's G query heads, (64, G, 1).
+  const uint32_t* block_members;
+  CUtensorMap tmap_q1;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
+// The swapped-orientation prefill kernel (bf16 / fp16 K/V, G a multiple of 8
+// and at most 64, tile_tokens * G <= 256, tile_tokens <= 32, no splits).
+cudaError_t launch_prefill_swapped(const PrefillArgs& a, cudaStream_t s);
 int device_sm_count();
 // Raises `kernel`'s dynamic shared-memory limit to at least `bytes` on the
 // current device; the driver call is made once per (kernel, device, size).

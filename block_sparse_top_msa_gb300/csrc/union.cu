@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(kUnionThreads)
   int* keys = scratch + nt + 2;                // P
   int* ulist = keys + P;                       // cap
   uint32_t* mem = reinterpret_cast<uint32_t*>(ulist + a.cap);  // W * words
+  uint32_t* bmem = mem + a.tile_tokens * a.words;              // cap (block_members only)
   __shared__ int s_ulen;
 
   grid_dependents_launch();
@@ -43,6 +44,8 @@ __global__ void __launch_bounds__(kUnionThreads)
     for (int j = tid; j < a.cap; j += nt) a.union_blocks[base * a.cap + j] = -1;
     for (int j = tid; j < a.tile_tokens * a.words; j += nt)
       a.member[base * a.tile_tokens * a.words + j] = 0u;
+    if (a.block_members != nullptr)
+      for (int j = tid; j < a.cap; j += nt) a.block_members[base * a.cap + j] = 0u;
     if (a.tile_info != nullptr && h == 0 && tid < 2) a.tile_info[2 * tile + tid] = -1;
     return;
   }
@@ -52,6 +55,8 @@ __global__ void __launch_bounds__(kUnionThreads)
   int nblk = (lk + kBlk - 1) / kBlk;
   if (a.seqused_k && nblk > a.max_pages) nblk = a.max_pages;
   const int nw = min(a.tile_tokens, end - t0);
+  if (a.block_members != nullptr)
+    for (int j = tid; j < a.cap; j += nt) bmem[j] = 0u;
 
   // Usable ids of the tile's rows; everything else sorts to the end.
   for (int i = tid; i < P; i += nt) {
@@ -125,12 +130,15 @@ __global__ void __launch_bounds__(kUnionThreads)
       if (ulist[mid] < id) lo = mid + 1; else hi = mid;
     }
     atomicOr(&mem[w * a.words + (lo >> 5)], 1u << (lo & 31));
+    if (a.block_members != nullptr) atomicOr(&bmem[lo], 1u << w);
   }
   __syncthreads();
   if (tid == 0) a.union_len[base] = ulen;
   for (int j = tid; j < a.cap; j += nt) a.union_blocks[base * a.cap + j] = j < ulen ? ulist[j] : -1;
   for (int j = tid; j < a.tile_tokens * a.words; j += nt)
     a.member[base * a.tile_tokens * a.words + j] = mem[j];
+  if (a.block_members != nullptr)
+    for (int j = tid; j < a.cap; j += nt) a.block_members[base * a.cap + j] = bmem[j];
   if (a.tile_info != nullptr && h == 0 && tid == 0) {
     a.tile_info[2 * tile] = t0;
     a.tile_info[2 * tile + 1] = b;
@@ -147,6 +155,7 @@ __global__ void __launch_bounds__(1024) build_union_small_kernel(UnionArgs a) {
   int* scratch = smem_i;             // nt + 2 (tile lookup), then nt (sort exchange)
   int* ulist = scratch + nt + 2;     // cap
   uint32_t* mem = reinterpret_cast<uint32_t*>(ulist + a.cap);  // W * words
+  uint32_t* bmem = mem + a.tile_tokens * a.words;              // cap (block_members only)
   __shared__ int s_warp[32];
   __shared__ int s_ulen;
 
@@ -160,6 +169,8 @@ __global__ void __launch_bounds__(1024) build_union_small_kernel(UnionArgs a) {
     for (int j = tid; j < a.cap; j += nt) a.union_blocks[base * a.cap + j] = -1;
     for (int j = tid; j < a.tile_tokens * a.words; j += nt)
       a.member[base * a.tile_tokens * a.words + j] = 0u;
+    if (a.block_members != nullptr)
+      for (int j = tid; j < a.cap; j += nt) a.block_members[base * a.cap + j] = 0u;
     if (a.tile_info != nullptr && h == 0 && tid < 2) a.tile_info[2 * tile + tid] = -1;
     return;
   }
@@ -170,6 +181,8 @@ __global__ void __launch_bounds__(1024) build_union_small_kernel(UnionArgs a) {
   if (a.seqused_k && nblk > a.max_pages) nblk = a.max_pages;
   const int nw = min(a.tile_tokens, end - t0);
   const int n = a.tile_tokens * a.topk;
+  if (a.block_members != nullptr)
+    for (int j = tid; j < a.cap; j += nt) bmem[j] = 0u;
 
   // This thread's id (usable ids only; the rest sort to the end).
   int key = INT_MAX;
@@ -234,12 +247,15 @@ __global__ void __launch_bounds__(1024) build_union_small_kernel(UnionArgs a) {
       if (ulist[mid] < my_id) lo = mid + 1; else hi = mid;
     }
     atomicOr(&mem[my_w * a.words + (lo >> 5)], 1u << (lo & 31));
+    if (a.block_members != nullptr) atomicOr(&bmem[lo], 1u << my_w);
   }
   __syncthreads();
   if (tid == 0) a.union_len[base] = ulen;
   for (int j = tid; j < a.cap; j += nt) a.union_blocks[base * a.cap + j] = j < ulen ? ulist[j] : -1;
   for (int j = tid; j < a.tile_tokens * a.words; j += nt)
     a.member[base * a.tile_tokens * a.words + j] = mem[j];
+  if (a.block_members != nullptr)
+    for (int j = tid; j < a.cap; j += nt) a.block_members[base * a.cap + j] = bmem[j];
   if (a.tile_info != nullptr && h == 0 && tid == 0) {
     a.tile_info[2 * tile] = t0;
     a.tile_info[2 * tile + 1] = b;
@@ -249,13 +265,14 @@ __global__ void __launch_bounds__(1024) build_union_small_kernel(UnionArgs a) {
 }  // namespace
 
 cudaError_t launch_build_union(const UnionArgs& a, cudaStream_t s) {
+  if (a.block_members != nullptr && a.tile_tokens > 32) return cudaErrorInvalidValue;
   const int n = a.tile_tokens * a.topk;
   int P = 1;
   while (P < n) P <<= 1;
   if (P <= 1024) {
     const int nt = P < 32 ? 32 : P;
-    const size_t smem =
-        sizeof(int) * ((size_t)nt + 2 + a.cap + (size_t)a.tile_tokens * a.words);
+    const size_t smem = sizeof(int) * ((size_t)nt + 2 + a.cap + (size_t)a.tile_tokens * a.words +
+                                       (a.block_members != nullptr ? (size_t)a.cap : 0));
     cudaError_t e = set_smem_limit((const void*)build_union_small_kernel, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.max_tiles, a.num_kv_heads);
@@ -263,7 +280,8 @@ cudaError_t launch_build_union(const UnionArgs& a, cudaStream_t s) {
     return cudaGetLastError();
   }
   const size_t smem =
-      sizeof(int) * ((size_t)kUnionThreads + 2 + P + a.cap + (size_t)a.tile_tokens * a.words);
+      sizeof(int) * ((size_t)kUnionThreads + 2 + P + a.cap + (size_t)a.tile_tokens * a.words +
+                     (a.block_members != nullptr ? (size_t)a.cap : 0));
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   cudaError_t e = set_smem_limit((const void*)build_union_kernel, (int)smem);
   if (e != cudaSuccess) return e;

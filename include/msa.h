@@ -305,6 +305,50 @@ msa_status_t msa_build_union(const int32_t* q2k_indices, int topk, const int32_t
 int msa_union_tile_tokens(int num_qo_heads, int num_kv_heads);
 
 /*
+ * msa_build_union with one more output, for tile_tokens <= 32:
+ *   block_members[h, tau, 0:cap]   device uint32; bit w set iff the tile's
+ *                                  token w has union_blocks[h, tau, j] usable
+ *                                  in its row (the member bits transposed);
+ *                                  0 past union_len
+ * This is the union metadata of the forward's swapped-orientation kernel
+ * (see msa_prefill_tile_tokens), which walks each union block's member
+ * tokens. Same arguments and errors as msa_build_union otherwise;
+ * tile_tokens > 32 or a NULL block_members is MSA_INVALID_ARG.
+ */
+msa_status_t msa_build_union_block_members(
+    const int32_t* q2k_indices, int topk, const int32_t* cu_seqlens_q,
+    const int32_t* cu_seqlens_k, const int32_t* seqused_k, int max_pages, int batch, int total_q,
+    int num_kv_heads, int causal, int tile_tokens, int max_tiles, int32_t* union_len,
+    int32_t* union_blocks, uint32_t* member, uint32_t* block_members, int32_t* tile_info,
+    cudaStream_t stream);
+
+/*
+ * Tokens per query tile of the attention kernel msa_sparse_attention_fwd
+ * uses for these sizes and K/V dtype under the current route (see
+ * msa_set_prefill_route; an E4M3 call on its bf16-copy route counts as
+ * MSA_BF16). Two kernels compute the same result:
+ *   - the union-tile kernel: floor(128 / G) tokens per tile (128 rows = one
+ *     MMA tile), each tile's rows walking its whole union; every call by
+ *     default;
+ *   - the swapped-orientation kernel: min(32, 256 / G) tokens per tile, the
+ *     MMAs' N being only the member rows of each union block; 16-bit K/V and
+ *     G a multiple of 8 up to 64, when route 2 is set.
+ * Both are capped at max_seqlen_q. Returns 0 for invalid sizes.
+ */
+int msa_prefill_tile_tokens(int batch, int total_q, int num_qo_heads, int num_kv_heads, int topk,
+                            int max_seqlen_q, msa_dtype_t kv_dtype);
+
+/*
+ * Testing and benchmarking: which attention kernel later forward calls use.
+ * 0 (the default) the faster one as measured (at present the union-tile
+ * kernel everywhere); 1 always the union-tile kernel; 2 the
+ * swapped-orientation kernel wherever it applies (16-bit K/V, G a multiple
+ * of 8 up to 64). Process-wide, not thread-safe. Other values:
+ * MSA_INVALID_ARG.
+ */
+msa_status_t msa_set_prefill_route(int route);
+
+/*
  * Waits for `stream`, then returns and clears the library's device fault word
  * of the current device in *fault (0 = none). Kernels never trap: a wait that
  * exceeds its time limit (2 s), or an internal capacity check, sets a bit here
@@ -340,8 +384,9 @@ msa_status_t msa_selftest_wait_timeout(unsigned int timeout_us, cudaStream_t str
  * msa_sparse_decode_noalloc_scratch_limit() returns the array size.
  *
  * The first call on a device looks up the array's device address (with that
- * device current) and caches it; make that first call before any stream
- * capture. All calls share the one array and it keeps the previous call's
+ * device current) and caches it for the life of the process; make that first
+ * call before any stream capture, and do not use the library across a
+ * cudaDeviceReset of that device (the cached address would be stale). All calls share the one array and it keeps the previous call's
  * contents (the forward needs no initialised workspace); calls whose work
  * overlaps on the GPU race on the array, so callers must order them.
  */
