@@ -10,34 +10,48 @@
 // tile over the union computes mostly masked products. Here the roles are
 // swapped: for each union block, the MMA's M is the block's 128 keys (QK) or
 // the 128 head dimensions (PV), and N is only the query rows that selected
-// the block (member rows, gathered), 16 to 64 per MMA. Per block the SM then
-// moves the block's K and V in once and does MMA work in proportion to its
-// member rows, and a tile can hold more tokens (32 x 8 heads = 256 rows),
-// so each K/V block brought in from L2 serves more rows.
+// the block (member rows, gathered), 16 to 64 per MMA. The MMA work then
+// follows the member rows, and a tile holds more tokens (32 x 8 heads = 256
+// rows), so each K/V block brought in from L2 serves more rows.
 //
 // Work item: a query tile of W tokens (W * G <= 256 rows, row r = token
-// r / G, head r % G of the KV head's group) and a KV head. Per union block u
-// with member tokens M_u, in chunks of at most 64 member rows:
-//   Q producer   : TMA-gathers the member tokens' G query rows into a
-//                  K-major buffer QB (N rows, N = 16 * ceil(|rows| / 16));
+// r / G, head r % G of the KV head's group) and a KV head. Its stream of
+// chunks: per union block with member tokens M_u, chunks of at most 64
+// member rows. Roles:
 //   K / V warps  : TMA the block's K and V tiles into two-slot rings (flat
-//                  rows cu_k[b] + 128 id, or page page_table[b, id]);
-//   MMA warp     : S^T = K_u QB^T (M = 128 keys, fp32 in TMEM), then, after
-//                  the softmax, D = V_u^T P (M = 128 dims, A MN-major) into
-//                  the same TMEM columns;
-//   softmax warps: thread = key (TMEM lane), columns = member rows; mask
-//                  keys past each row's causal limit / the sequence end,
-//                  column maxima and sums by shuffle transposes and an
-//                  exchange across the four lane quarters, running max per
-//                  row (O rescaled lazily, only when the max grows by more
-//                  than 2^8), P = 2^(s * scale * log2 e - m) written as
-//                  bf16 / fp16 over QB (the PV's B operand);
+//                  rows cu_k[b] + 128 id, or page page_table[b, id]); the K
+//                  warp also hands out the work items;
+//   Q warp       : walks the chunk stream, publishes each chunk's record
+//                  and column table (row and key limit per column) in
+//                  shared memory, and TMA-gathers the member tokens' G query
+//                  rows into a K-major buffer QB (N = 16 * ceil(rows / 16));
+//   MMA warp     : follows the records; each step issues S^T = K_u QB^T of
+//                  chunk g + 2 (M = 128 keys, fp32 in TMEM) and D = V_u^T P
+//                  of chunk g (M = 128 dims, A and B MN-major) with their K
+//                  steps interleaved;
+//   softmax warps: two teams of four (one warp per key quarter = TMEM lane
+//                  quarter) take alternate chunks: mask keys past each
+//                  column's limit, column maxima by shuffle transposes and an
+//                  exchange across the quarters, the running max per row
+//                  (updated in chunk order, handed between the teams per
+//                  quarter; O rescaled lazily, only when the max grows by
+//                  more than 2^8), P = 2^(s * scale * log2 e - m) written
+//                  as bf16 / fp16 over QB, and per-quarter column sums;
 //   merge warps  : thread = head dimension; O^T[:, row] = alpha * O^T[:, row]
-//                  + D[:, column] for each member row, O^T (d x 256 rows,
-//                  fp32) resident in TMEM for the whole item; at the end of
-//                  the item out = O / l and the natural-log LSE.
+//                  + D[:, column] for each member row and l[row] = alpha *
+//                  l[row] + column sum, O^T (d x 256 rows, fp32) resident in
+//                  TMEM for the whole item; at the end of the item out = O / l
+//                  and the natural-log LSE.
 // Rows whose token did not select a block get nothing from it, so each
 // row's result is exactly its own blocks' softmax attention.
+//
+// Measured on the flat varlen prefill (2 x 32768, 64/8 heads, top-16) it
+// takes 24 ms against 17.9 ms for the union-tile kernel (prefill.cu): per
+// chunk of about 32 member rows the softmax team needs about 3400 cycles
+// from S^T to P, and with QK two chunks ahead that latency sets the pace,
+// although the MMAs and the K/V loads per chunk would take about a third of
+// it. The forward therefore runs the union-tile kernel unless route 2 is
+// chosen (msa_set_prefill_route).
 #include <math.h>
 
 #include "common.cuh"
@@ -213,12 +227,15 @@ MSA_DEV SwItem sw_item_at(const PrefillArgs& a, int i) {
 
 // Walks an item's chunks: union blocks with at least one member token, each
 // split into chunks of at most `tpc` member tokens (lowest tokens first).
-// g counts chunks and j counts blocks over the CTA's whole stream; every
-// role walks the same sequence.
+// g counts chunks and j counts blocks over the CTA's whole stream. Called
+// by all 32 lanes of a warp: the union list is read 32 blocks at a time,
+// one block per lane, and handed out by shuffles.
 struct Chunks {
   const uint32_t* bm;
   const int32_t* ul;
-  int n_union, u;
+  int n_union, u, wbase;
+  uint32_t w_bm;   // this lane's block of the current window
+  int w_ul;
   uint32_t rest;  // members of block u not yet in a chunk
   uint32_t cm;    // the current chunk's member tokens
   int ntok, N, blk;
@@ -232,6 +249,7 @@ MSA_DEV void chunks_item(Chunks& c, const PrefillArgs& a, const SwItem& it) {
   c.ul = a.union_blocks + unit * a.cap;
   c.n_union = it.n_union;
   c.u = -1;
+  c.wbase = -32;
   c.rest = 0u;
 }
 
@@ -239,9 +257,15 @@ MSA_DEV bool chunks_next(Chunks& c, int tpc, int G) {
   c.first = false;
   while (c.rest == 0u) {
     if (++c.u >= c.n_union) return false;
-    c.rest = __ldg(c.bm + c.u);
+    if (c.u >= c.wbase + 32) {
+      c.wbase = c.u;
+      const int v = c.u + (int)(threadIdx.x & 31);
+      c.w_bm = v < c.n_union ? __ldg(c.bm + v) : 0u;
+      c.w_ul = v < c.n_union ? __ldg(c.ul + v) : 0;
+    }
+    c.rest = __shfl_sync(0xffffffffu, c.w_bm, c.u - c.wbase);
     if (c.rest != 0u) {
-      c.blk = __ldg(c.ul + c.u);
+      c.blk = __shfl_sync(0xffffffffu, c.w_ul, c.u - c.wbase);
       c.first = true;
       ++c.j;
     }
@@ -525,17 +549,10 @@ __global__ void __launch_bounds__(kSwThreads, 1)
       chunks_item(c, a, it);
       while (chunks_next(c, tpc, G)) {
         const int buf = c.g & (kSwBuf - 1), ts = c.g & (kColSlots - 1);
-        // Last chunk of the item: no members left in this block and none in
-        // the blocks after it.
-        bool item_end = false;
-        if (c.rest == 0u) {
-          item_end = true;
-          for (int u = c.u + 1; u < c.n_union; ++u)
-            if (__ldg(c.bm + u) != 0u) {
-              item_end = false;
-              break;
-            }
-        }
+        // Last chunk of the item: the last chunk of its last union block
+        // (every union block has a member token: the union holds exactly the
+        // ids some token of the tile can use).
+        const bool item_end = c.rest == 0u && c.u == c.n_union - 1;
         if (!take_buffer(c.g)) {
           ok = false;
           break;

@@ -89,3 +89,25 @@ def test_noalloc_refuses_problems_larger_than_its_scratch(msa):
     st = L.msa_sparse_decode_noalloc(A, A, A, A, 16, A, None, 4, 4, A, 1, 8, 8, 1, 128, 8, 1, 0.0,
                                      A, None, None)
     assert msa.status_string(st) == "MSA_INVALID_ARG"
+
+
+@pytest.mark.gpu
+def test_noalloc_empty_call_returns_ok(msa):
+    """A call with no query rows (total_q = 0) is valid, as it is for the
+    regular forward: MSA_OK, nothing launched, nothing written."""
+    dev = "cuda:0"
+    inp = _decode_inputs(3, 1, [500, 300], 16, 2, 4, dev)
+    q = inp["q"][:0]
+    out = torch.empty_like(q)
+    L = msa.lib()
+    st = L.msa_sparse_decode_noalloc(
+        C.c_void_p(inp["q"].data_ptr()), C.c_void_p(inp["k"].data_ptr()),
+        C.c_void_p(inp["v"].data_ptr()), C.c_void_p(inp["q2k_indices"].data_ptr()), 4,
+        C.c_void_p(torch.zeros(3, dtype=torch.int32, device=dev).data_ptr()),
+        C.c_void_p(inp["page_table"].data_ptr()), inp["page_table"].shape[1], inp["k"].shape[0],
+        C.c_void_p(inp["seqused_k"].data_ptr()), 2, 0, 16, 2, 128, 1, 1, 0.0,
+        C.c_void_p(inp["q"].data_ptr()), None, None)
+    torch.cuda.synchronize()
+    assert msa.status_string(st) == "MSA_OK"
+    fault_clear(msa)
+    del out
