@@ -451,14 +451,25 @@ def bench_decode(msa, device, flush, seed=0, small=False, sqs=(1, 4), reps=7):
 
         for _ in range(3):
             call()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        # The whole call between events recorded around it (nothing between
+        # its kernels, so the attention kernel's early start is kept), then
+        # the attention launch alone from the library's own events.
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ts, ta = [], []
+        for _ in range(reps):
+            flush.fill_(1)
+            torch.cuda._sleep(200_000)  # keeps the GPU busy while the host enqueues the call
+            e0.record()
+            call()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         for _ in range(reps):
             flush.fill_(1)
             msa.msa_set_timing_events(ev)
             call()
             ev[2].synchronize()
-            ts.append(ev[0].elapsed_time(ev[2]) * 1e-3)
             ta.append(ev[1].elapsed_time(ev[2]) * 1e-3)
         msa.msa_set_timing_events(None)
         t, t_attn = statistics.median(ts), statistics.median(ta)
@@ -521,14 +532,25 @@ def bench_decode_nvfp4(msa, device, flush, seed=0, sqs=(1, 4), reps=7, small=Fal
 
         for _ in range(3):
             call()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        # The whole call between events recorded around it (nothing between
+        # its kernels, so the attention kernel's early start is kept), then
+        # the attention launch alone from the library's own events.
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         ts, ta = [], []
+        for _ in range(reps):
+            flush.fill_(1)
+            torch.cuda._sleep(200_000)  # keeps the GPU busy while the host enqueues the call
+            e0.record()
+            call()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e-3)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         for _ in range(reps):
             flush.fill_(1)
             msa.msa_set_timing_events(ev)
             call()
             ev[2].synchronize()
-            ts.append(ev[0].elapsed_time(ev[2]) * 1e-3)
             ta.append(ev[1].elapsed_time(ev[2]) * 1e-3)
         msa.msa_set_timing_events(None)
         t, t_attn = statistics.median(ts), statistics.median(ta)
@@ -809,6 +831,8 @@ def main():
                     help="profiling case: prefill only, 1 x 8192 tokens, 64/8 heads, top-16")
     ap.add_argument("--profile-decode", type=int, default=0, metavar="SQ",
                     help="profiling case: paged decode only, 64 requests, seqlen_q SQ")
+    ap.add_argument("--profile-decode-full", action="store_true",
+                    help="profiling case: the full paged decode only (128 requests), s_q 1 and 4")
     ap.add_argument("--profile-e4m3", action="store_true",
                     help="profiling case: the E4M3 K/V varlen prefill only")
     ap.add_argument("--profile-nvfp4-small", action="store_true",
@@ -836,6 +860,11 @@ def main():
         r = bench_decode(msa, device, flush, small=True, sqs=(args.profile_decode,),
                          reps=args.steps)
         print(json.dumps({"profile_decode": r}))
+        return 0
+    if args.profile_decode_full:
+        flush = l2_flush_buffer(device)
+        print(json.dumps({"profile_decode_full": bench_decode(msa, device, flush,
+                                                              reps=max(args.steps, 3))}))
         return 0
     if args.profile_nvfp4_small:
         flush = l2_flush_buffer(device)

@@ -371,6 +371,7 @@ struct ForwardPlan {
   UnionArgs u{};
   PrefillArgs a{};
   bool swapped = false;  // the swapped-orientation prefill kernel, else the union-tile kernel
+  bool skip_union = false;  // direct mode: the attention kernel builds one-token unions itself
 };
 
 // The swapped-kernel part of a forward plan (arguments already checked).
@@ -610,6 +611,16 @@ msa_status_t build_forward(
   a.part_o = reinterpret_cast<float*>(ws + L.off_part_o);
   a.part_ml = reinterpret_cast<float*>(ws + L.off_part_ml);
   a.item_counter = u.item_counter;
+  a.q2k = q2k_indices;
+  a.topk = topk;
+  // One-token tiles (decode with seqlen_q 1, or G >= 128): the attention
+  // kernel derives each tile's union from the token's own row (bf16 / fp16
+  // instance; the E4M3 / NVFP4 converter instance keeps the union kernel).
+  a.direct = (L.W == 1 && topk <= 32 && esize == 2) ? 1 : 0;
+  plan->skip_union = a.direct != 0;
+  // The counter reset before a direct launch is an ordinary launch, so every
+  // earlier kernel (a decode pass included) has completed when it starts.
+  a.wait_late = a.direct;
   return MSA_OK;
 }
 
@@ -690,7 +701,8 @@ msa_status_t launch_forward(const ForwardPlan& p, cudaStream_t stream) {
   if (e != cudaSuccess) return MSA_CUDA_ERROR;
   e = launch_page_decode(p.pd, stream);
   if (e != cudaSuccess) return MSA_CUDA_ERROR;
-  e = launch_build_union(p.u, stream);
+  e = p.skip_union ? launch_reset_counter(p.a.item_counter, stream)
+                   : launch_build_union(p.u, stream);
   if (e != cudaSuccess) return MSA_CUDA_ERROR;
   mark(1, stream);
   e = p.swapped ? launch_prefill_swapped(p.a, stream) : launch_prefill(p.a, stream);

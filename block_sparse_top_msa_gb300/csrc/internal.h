@@ -38,6 +38,9 @@ struct UnionArgs {
   uint32_t* block_members;
 };
 cudaError_t launch_build_union(const UnionArgs& a, cudaStream_t s);
+// Zeroes the attention kernel's work counter in a one-thread kernel that
+// lets its programmatic dependent start at once.
+cudaError_t launch_reset_counter(int32_t* counter, cudaStream_t s);
 
 struct TopkArgs {
   const float* scores;
@@ -112,6 +115,18 @@ struct PrefillArgs {
   // box is one token's G query heads, (64, G, 1).
   const uint32_t* block_members;
   CUtensorMap tmap_q1;
+  // One-token tiles (tile_tokens == 1, topk <= 32) may skip the union
+  // kernel: with `direct` set, the attention kernel's item setup filters,
+  // sorts and deduplicates the token's own q2k row (every union entry is
+  // then a member) and writes union_len, union_blocks and tile_info itself.
+  const int32_t* q2k;
+  int topk;
+  int direct;
+  // The preceding kernel only zeroes item_counter (launch_reset_counter, an
+  // ordinary launch, so every other input was complete before it began): the
+  // attention kernel waits for it only before its first claim from the
+  // counter.
+  int wait_late;
 };
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t s);
 // The swapped-orientation prefill kernel (bf16 / fp16 K/V, G a multiple of 8

@@ -311,6 +311,119 @@ MSA_DEV Item item_at(const PrefillArgs& a, int i, int2 ti) {
   return it;
 }
 
+// Union metadata load: read-only path when the union kernel wrote it before
+// the launch, L2 when this launch's own item setup wrote it (direct mode).
+MSA_DEV int32_t meta_ld(const int32_t* p, bool direct) { return direct ? __ldcg(p) : __ldg(p); }
+MSA_DEV uint32_t meta_ld(const uint32_t* p, bool direct) { return direct ? __ldcg(p) : __ldg(p); }
+
+// Sequence holding packed query row t: the b with cu_q[b] <= t < cu_q[b + 1],
+// returned with those two offsets. The first probe assumes equal query
+// lengths (exact for a decode batch); otherwise a binary search for the last
+// b with cu_q[b] <= t.
+MSA_DEV int find_sequence(const int32_t* cu_q, int batch, int total_q, int t, int& q0, int& q1) {
+  const int g = min(batch - 1, (int)((long long)t * batch / max(total_q, 1)));
+  q0 = __ldcg(cu_q + g);
+  q1 = __ldcg(cu_q + g + 1);
+  if (q0 <= t && t < q1) return g;
+  int lo = 0, hi = batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldcg(cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  q0 = __ldcg(cu_q + lo);
+  q1 = __ldcg(cu_q + lo + 1);
+  return lo;
+}
+
+// Work item i of a one-token-tile launch without the union kernel (direct
+// mode): the tile is query row t0 = tile, and its union is that token's own
+// selection: the ids of its q2k row (KV head h) that are usable (0 <= id <
+// number of blocks, and id * 128 <= the token's position when causal),
+// ascending and without repeats, the set the union kernel would produce for a
+// one-token tile. The list, its length and the tile's (t0, b) are written to
+// the union arrays for the other roles (which read them after the item is
+// published) and the merge kernel; every split of a unit writes the same
+// values. One thread; two dependent rounds of loads (the row with the
+// sequence probe, then the sequence's key length).
+MSA_DEV Item direct_item(const PrefillArgs& a, int i) {
+  constexpr int kN = 32;  // topk <= 32
+  Item it;
+  int unit;
+  if (i < a.whole_units) {
+    unit = i;
+    it.split = 0;
+    it.tail = -1;
+  } else {
+    const int j = i - a.whole_units;
+    it.tail = j / a.splits;
+    it.split = j - it.tail * a.splits;
+    unit = a.whole_units + it.tail;
+  }
+  it.h = unit / a.max_tiles;
+  it.tile = a.max_tiles - 1 - (unit - it.h * a.max_tiles);
+  it.t0 = it.tile;
+  it.p_begin = it.tail < 0 ? 0 : it.split * a.pps;
+  const int32_t* row = a.q2k + ((size_t)it.h * a.total_q + it.t0) * a.topk;
+  int key[kN];
+#pragma unroll
+  for (int j = 0; j < kN; ++j) key[j] = j < a.topk ? __ldcg(row + j) : -1;
+  int q1;
+  it.b = find_sequence(a.cu_q, a.batch, a.total_q, it.t0, it.seq_q0, q1);
+  it.lq = q1 - it.seq_q0;
+  int nblk;
+  if (a.paged) {
+    it.kv0 = 0;
+    it.lk = __ldcg(a.seqused_k + it.b);
+    nblk = min((it.lk + kBlk - 1) / kBlk, a.max_pages);
+  } else {
+    it.kv0 = __ldcg(a.cu_k + it.b);
+    it.lk = __ldcg(a.cu_k + it.b + 1) - it.kv0;
+    nblk = (it.lk + kBlk - 1) / kBlk;
+  }
+  const long long pos = (long long)it.lk - it.lq + (it.t0 - it.seq_q0);
+  bool sorted = true;
+#pragma unroll
+  for (int j = 0; j < kN; ++j) {
+    const int id = key[j];
+    key[j] = (id < 0 || id >= nblk || (a.causal && (long long)id * kBlk > pos)) ? INT_MAX : id;
+    if (j > 0) sorted = sorted && key[j - 1] <= key[j];
+  }
+  if (!sorted) {
+    // Bitonic sorting network, ascending.
+#pragma unroll
+    for (int k = 2; k <= kN; k <<= 1) {
+#pragma unroll
+      for (int s = k >> 1; s > 0; s >>= 1) {
+#pragma unroll
+        for (int x = 0; x < kN; ++x) {
+          const int y = x ^ s;
+          if (y > x) {
+            const int lo = min(key[x], key[y]), hi = max(key[x], key[y]);
+            const bool up = (x & k) == 0;
+            key[x] = up ? lo : hi;
+            key[y] = up ? hi : lo;
+          }
+        }
+      }
+    }
+  }
+  // The union arrays are indexed (KV head, tile), like the union kernel's.
+  const size_t slot = (size_t)it.h * a.max_tiles + it.tile;
+  int32_t* dst = const_cast<int32_t*>(a.union_blocks) + slot * a.cap;
+  int n = 0;
+#pragma unroll
+  for (int j = 0; j < kN; ++j) {
+    if (key[j] != INT_MAX && (j == 0 || key[j] != key[j - 1])) dst[n++] = key[j];
+  }
+  const_cast<int32_t*>(a.union_len)[slot] = n;
+  int32_t* ti = const_cast<int32_t*>(a.tile_info) + 2 * it.tile;
+  ti[0] = it.t0;
+  ti[1] = it.b;
+  it.n_union = n;
+  it.n = it.tail < 0 ? n : max(0, min(n, it.p_begin + a.pps) - it.p_begin);
+  return it;
+}
+
 // Slot index and phase parity of a position in a ring of N slots, advanced
 // one step at a time (no divisions on the MMA issue path).
 template <int N>
@@ -436,7 +549,10 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   const uint32_t tbase = sm.tmem_base;
   // Everything above overlaps the tail of the union-metadata kernel; its
   // results are read only after this wait (programmatic dependent launch).
-  grid_dependency_wait();
+  // With wait_late, the kernel before this one only zeroes the work counter
+  // (all other inputs were complete before it started): only the K producer
+  // waits, before its first claim from the counter.
+  if (!a.wait_late) grid_dependency_wait();
   grid_dependents_launch();
 
   if (warp == R::kProducerWarp || warp == R::kVProducerWarp) {
@@ -462,19 +578,46 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       // ends, so SMs that run faster take more items. Items with nothing to do
       // are skipped, except a tile's first split when the tile has no usable
       // block (its rows are written as empty by the softmax warps).
+      // Launches that wait late (direct mode) take their first item before
+      // the kernel that zeroes the counter has been waited for.
       int claim = blockIdx.x;
+      // The claimed next item is set up (its loads) while this item's last
+      // blocks are in flight, right after a block's copies are issued.
+      Item pend{};
+      int pend_idx = -1;
+      bool want_pend = false;
+      // Loads item x's Q tile as the kk-th non-empty item's (slot kk % kQBuf).
+      auto load_q = [&](int kk, const Item& x) -> bool {
+        const int qb = kk % kQBuf;
+        if (kk >= kQBuf &&
+            !mbar_wait(&sm.q_empty[qb], ((kk / kQBuf) - 1) & 1, fault, kFaultWaitMma, abort))
+          return false;
+        mbar_expect_tx(&sm.q_full[qb], 2u * 128u * (uint32_t)(G * W));
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d(q_addr(qb, c), &a.tmap_q, &sm.q_full[qb], c * 64, x.h * G, x.t0);
+        return true;
+      };
+      bool dep_waited = !a.wait_late;
+      auto next_claim = [&](int) {
+        if (!dep_waited) {
+          grid_dependency_wait();
+          dep_waited = true;
+        }
+        return (int)gridDim.x + atomicAdd(a.item_counter, 1);
+      };
       for (int ni = 0; ok; ++ni) {
         Item it{};
         int i = -1;
         if (kq) {
           while (claim < a.num_items) {
             const int cand = claim;
-            it = item_at(a, cand, item_tile_info(a, cand));
+            if (cand == pend_idx) it = pend;
+            else it = a.direct ? direct_item(a, cand) : item_at(a, cand, item_tile_info(a, cand));
             if (it.t0 >= 0 && (it.n > 0 || (it.split == 0 && it.n_union == 0))) {
               i = cand;
               break;
             }
-            claim = (int)gridDim.x + atomicAdd(a.item_counter, 1);
+            claim = next_claim(claim);
           }
           const int slot = ni % kItemRing;
           if (ni >= kItemRing && !mbar_wait(&sm.item_empty[slot], ((ni / kItemRing) - 1) & 1, fault,
@@ -486,7 +629,10 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
           if (i >= 0) sm.item_ring[slot] = it;
           mbar_arrive(&sm.item_full[slot]);
           if (i < 0) break;
-          if (it.n <= kClaimAhead) claim = (int)gridDim.x + atomicAdd(a.item_counter, 1);
+          if (it.n <= kClaimAhead) {
+            claim = next_claim(claim);
+            want_pend = true;
+          }
         } else {
           i = read_item(ni, ok, it);
           if (!ok) break;
@@ -494,26 +640,29 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
           if (i < 0) break;
         }
         if (it.n == 0) continue;
-        if (kq) {
-          const int qb = k % kQBuf;
-          if (k >= kQBuf &&
-              !mbar_wait(&sm.q_empty[qb], ((k / kQBuf) - 1) & 1, fault, kFaultWaitMma, abort)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(&sm.q_full[qb], 2u * 128u * (uint32_t)(G * W));
-          for (int c = 0; c < 2; ++c)
-            tma_load_3d(q_addr(qb, c), &a.tmap_q, &sm.q_full[qb], c * 64, it.h * G, it.t0);
+        if (kq && !load_q(k, it)) {
+          ok = false;
+          break;
         }
         const int32_t* ulist =
             a.union_blocks + ((size_t)it.h * a.max_tiles + it.tile) * a.cap + it.p_begin;
+        // Union entries two blocks ahead, page entries one block ahead, so a
+        // block's copies never wait on a load chain.
+        const int32_t* prow = a.paged ? a.page_table + (size_t)it.b * a.max_pages : nullptr;
+        int id1 = meta_ld(ulist, a.direct);
+        int id2 = it.n > 1 ? meta_ld(ulist + 1, a.direct) : 0;
+        int pg1 = a.paged ? prow[id1] : 0;
         for (int u = 0; u < it.n; ++u, ++g) {
-          if (kq && it.n > kClaimAhead && u == it.n - kClaimAhead)
-            claim = (int)gridDim.x + atomicAdd(a.item_counter, 1);
-          const int blk = ulist[u];
-          int page = 0;
+          if (kq && it.n > kClaimAhead && u == it.n - kClaimAhead) {
+            claim = next_claim(claim);
+            want_pend = true;
+          }
+          const int blk = id1;
+          int page = pg1;
+          id1 = id2;
+          if (u + 2 < it.n) id2 = meta_ld(ulist + u + 2, a.direct);
+          if (a.paged && u + 1 < it.n) pg1 = prow[id1];
           if (a.paged) {
-            page = a.page_table[(size_t)it.b * a.max_pages + blk];
             // An unmapped page reads as zeros (out-of-range TMA box) and is masked.
             if (page < 0 || page >= a.num_pages) page = a.num_pages;
           }
@@ -565,6 +714,13 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
               else tma_load_3d(sm.k[ks][c], &a.tmap_k, &sm.k_full[ks], c * 64, it.h, row);
             }
             last_k[ks] = g;
+            if (want_pend) {
+              want_pend = false;
+              if (claim < a.num_items) {
+                pend = a.direct ? direct_item(a, claim) : item_at(a, claim, item_tile_info(a, claim));
+                pend_idx = claim;
+              }
+            }
           } else {
             const int vs = g % kVStages;
             if (g >= kVStages && !pv_wait(g - kVStages)) {
@@ -788,27 +944,27 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       const uint32_t* mrow = a.member + (unit * W + (active ? w : 0)) * a.words;
       const int32_t* ulist = a.union_blocks + unit * a.cap + it.p_begin;
       float m_ref = -INFINITY, l = 0.f;  // l: sum over this warp's columns
-      // Per-block metadata for block u, fetched one block ahead.
-      uint32_t mword = active ? __ldg(mrow + (it.p_begin >> 5)) : 0u;
-      int nblk_id = __ldg(ulist);
-      int npage_ok = 1;
-      if (a.paged) {
-        const int pg = __ldg(a.page_table + (size_t)it.b * a.max_pages + nblk_id);
-        npage_ok = pg >= 0 && pg < a.num_pages;
-      }
+      // Per-block metadata, loaded ahead so that no load waits on another in
+      // the block loop: union entries two blocks ahead, page entries one block
+      // ahead (kept raw until used). Direct mode: every union entry is the
+      // token's own (usable) block.
+      uint32_t mword = !active ? 0u : a.direct ? ~0u : __ldg(mrow + (it.p_begin >> 5));
+      const int32_t* prow = a.paged ? a.page_table + (size_t)it.b * a.max_pages : nullptr;
+      int id1 = meta_ld(ulist, a.direct);
+      int id2 = it.n > 1 ? meta_ld(ulist + 1, a.direct) : 0;
+      int pg1 = a.paged ? __ldg(prow + id1) : 0;
       for (int u = 0; u < it.n; ++u) {
         const int gg = g + u, bb = gg % kSBuf;
         const int upos = it.p_begin + u;  // position in the tile's union list
-        const int blk = nblk_id;
-        bool mem = active && ((mword >> (upos & 31)) & 1u) && npage_ok;
-        if (u + 1 < it.n) {
-          nblk_id = __ldg(ulist + u + 1);
-          if (a.paged) {
-            const int pg = __ldg(a.page_table + (size_t)it.b * a.max_pages + nblk_id);
-            npage_ok = pg >= 0 && pg < a.num_pages;
-          }
-          if (((upos + 1) & 31) == 0 && active) mword = __ldg(mrow + ((upos + 1) >> 5));
-        }
+        const int blk = id1;
+        const int pg = pg1;
+        id1 = id2;
+        if (u + 2 < it.n) id2 = meta_ld(ulist + u + 2, a.direct);
+        if (a.paged && u + 1 < it.n) pg1 = __ldg(prow + id1);
+        const bool page_ok = !a.paged || (pg >= 0 && pg < a.num_pages);
+        bool mem = active && ((mword >> (upos & 31)) & 1u) && page_ok;
+        if (u + 1 < it.n && ((upos + 1) & 31) == 0 && active && !a.direct)
+          mword = __ldg(mrow + ((upos + 1) >> 5));
         int lim = 127;
         if (mem) {
           long long last = (long long)it.lk - 1;
@@ -1016,12 +1172,18 @@ cudaError_t launch_dependent(Kernel kernel, dim3 grid, dim3 block, size_t smem, 
 // Combines the fp32 partials of the tail units whose union was split across
 // several work items: for each such unit and active row, with
 // M = max_s m_s, L = sum_s 2^(m_s - M) l_s, out = sum_s 2^(m_s - M) O_s / L and
-// lse = (M + log2 L) ln 2 (m in log2 units of the scaled logits). One warp per
-// (tail unit, row); each lane owns four of the 128 dims.
+// lse = (M + log2 L) ln 2 (m in log2 units of the scaled logits), M taken
+// as a running maximum over groups of four splits whose loads are issued
+// together. A split with no visible key (m = -inf) contributes nothing. One
+// warp per (tail unit, row); each lane owns four of the 128 dims.
 __global__ void __launch_bounds__(256) merge_splits_kernel(const __grid_constant__ PrefillArgs a) {
   // The union metadata read below is final before this launch may begin: the
   // attention kernel lets it launch only after waiting for the union kernel.
   // Only the partials need the wait, so it comes after the metadata loads.
+  // In direct mode the attention kernel writes the metadata; a one-token tile
+  // is its own query row (t0 = tile, one token), so only the union length is
+  // read, after the wait, together with the first splits' partials.
+  constexpr int kU = 4;
   const int warp_global = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (warp_global >= a.tail_units * a.rows_part) return;
@@ -1029,40 +1191,56 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const __grid_constant
   const int unit = a.whole_units + t;
   const int h = unit / a.max_tiles;  // same head-major order as item_at
   const int tile = a.max_tiles - 1 - (unit - h * a.max_tiles);
-  const int t0 = __ldg(a.tile_info + 2 * tile);
-  if (t0 < 0) return;
-  const int n_union = __ldg(a.union_len + (size_t)h * a.max_tiles + tile);
-  const int nsplit = (n_union + a.pps - 1) / a.pps;
-  if (nsplit <= 1) return;  // written directly by the attention kernel
   const int G = a.num_qo_heads / a.num_kv_heads;
-  const int b = __ldg(a.tile_info + 2 * tile + 1);
-  const int nw = min(a.tile_tokens, __ldg(a.cu_q + b + 1) - t0);
   const int w = row / G, gh = row - w * G;
-  if (row >= a.tile_tokens * G || w >= nw) return;
+  if (row >= a.tile_tokens * G) return;
+  int t0 = tile, n_union = 0;
+  if (!a.direct) {
+    t0 = __ldg(a.tile_info + 2 * tile);
+    if (t0 < 0) return;
+    n_union = __ldg(a.union_len + (size_t)h * a.max_tiles + tile);
+    if ((n_union + a.pps - 1) / a.pps <= 1) return;  // written directly by the attention kernel
+    const int b = __ldg(a.tile_info + 2 * tile + 1);
+    if (w >= min(a.tile_tokens, __ldg(a.cu_q + b + 1) - t0)) return;
+  }
   const size_t p0 = (size_t)t * a.splits * a.rows_part + row;
-  grid_dependency_wait();  // partials of the attention kernel launched just before
-  float M = -INFINITY;
-#pragma unroll 4
-  for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldg(a.part_ml + (p0 + (size_t)sp * a.rows_part) * 2));
-  float L = 0.f;
+  grid_dependency_wait();  // partials (and, in direct mode, metadata) of the attention kernel
+  if (a.direct) n_union = __ldcg(a.union_len + (size_t)h * a.max_tiles + tile);
+  float M = -INFINITY, L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-#pragma unroll 4
-    for (int sp = 0; sp < nsplit; ++sp) {
-      const size_t pr = p0 + (size_t)sp * a.rows_part;
-      const float2 ml = __ldg(reinterpret_cast<const float2*>(a.part_ml) + pr);
-      const float4 ov = __ldg(reinterpret_cast<const float4*>(a.part_o + pr * 128) + lane);
-      // A split with no visible key (m = -inf) contributes nothing; its O
-      // slot is loaded with the others but not used.
-      if (ml.x != -INFINITY) {
-        const float f = ex2(ml.x - M);
-        L += f * ml.y;
-        acc.x += f * ov.x;
-        acc.y += f * ov.y;
-        acc.z += f * ov.z;
-        acc.w += f * ov.w;
-      }
+  // Loads of a group run ahead of the union length (bounded by the launch's
+  // split count); splits past the unit's own count are ignored.
+  for (int s0 = 0; s0 < a.splits; s0 += kU) {
+    float2 ml[kU];
+    float4 ov[kU];
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const size_t pr = p0 + (size_t)min(s0 + j, a.splits - 1) * a.rows_part;
+      ml[j] = __ldcg(reinterpret_cast<const float2*>(a.part_ml) + pr);
+      ov[j] = __ldcg(reinterpret_cast<const float4*>(a.part_o + pr * 128) + lane);
     }
+    const int nsplit = (n_union + a.pps - 1) / a.pps;
+    if (nsplit <= 1) return;  // direct mode: written directly by the attention kernel
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      if (s0 + j >= nsplit || ml[j].x == -INFINITY) continue;
+      if (ml[j].x > M) {
+        const float r = ex2(M - ml[j].x);  // 0 while M is -inf (L and acc are 0 then)
+        L *= r;
+        acc.x *= r;
+        acc.y *= r;
+        acc.z *= r;
+        acc.w *= r;
+        M = ml[j].x;
+      }
+      const float f = ex2(ml[j].x - M);
+      L += f * ml[j].y;
+      acc.x += f * ov[j].x;
+      acc.y += f * ov[j].y;
+      acc.z += f * ov[j].z;
+      acc.w += f * ov[j].w;
+    }
+    if (s0 + kU >= nsplit) break;
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const size_t orow = (size_t)(t0 + w) * a.num_qo_heads + (size_t)h * G + gh;

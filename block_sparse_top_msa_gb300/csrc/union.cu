@@ -262,7 +262,20 @@ __global__ void __launch_bounds__(1024) build_union_small_kernel(UnionArgs a) {
   }
 }
 
+__global__ void __launch_bounds__(32) reset_counter_kernel(int32_t* counter) {
+  grid_dependents_launch();
+  if (threadIdx.x == 0) *counter = 0;
+  // Completes only after the grids it depends on (if launched as a
+  // dependent), so its completion implies theirs.
+  grid_dependency_wait();
+}
+
 }  // namespace
+
+cudaError_t launch_reset_counter(int32_t* counter, cudaStream_t s) {
+  reset_counter_kernel<<<1, 32, 0, s>>>(counter);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_build_union(const UnionArgs& a, cudaStream_t s) {
   if (a.block_members != nullptr && a.tile_tokens > 32) return cudaErrorInvalidValue;
