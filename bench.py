@@ -316,14 +316,17 @@ def bench_prefill(msa, args, device, world, rank):
         spec=spec, inp=inp, flops=flops, flops_block=flops_block, flops_exec=flops_exec,
         step_s=step_s, wall_s=wall, attn_s=attn_s, meta_s=statistics.mean(meta_times),
         value=aggregate_value(flops, world, step_s) / 1e12, clocks=clk.summary(), fault=fault,
+        # The timed region is a fraction of a second of 18 ms launches: the
+        # burst bf16 figure is the denominator (the sustained one is listed).
         roofline={"bound": "tensor", "achieved": round(achieved, 2),
-                  "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                  "frac": round(achieved / pk["bf16_sus"], 4),
+                  "peak": pk["bf16"], "unit": "TFLOP/s",
+                  "frac": round(achieved / pk["bf16"], 4),
+                  "peak_sustained": pk["bf16_sus"],
                   "traffic": None if args.profile_small else measured_traffic(),
                   "traffic_source": TRAFFIC_MEASURED["profile"],
                   "algorithmic_bytes": int(alg_bytes),
                   "kernel": "prefill_kernel<bf16>",
-                  "peak_kind": f"bf16_tflops_sustained ({pk['source']})",
+                  "peak_kind": f"bf16_tflops, burst ({pk['source']})",
                   "achieved_is": "algorithmic FLOP per launch / mean launch time"},
         executed_tflops=flops_exec / attn_s / 1e12,
         work_efficiency=flops / flops_exec,
@@ -618,8 +621,8 @@ def bench_nvfp4_prefill(msa, device, flush, seed=0, reps=3):
             "value": round(flops / t / 1e12, 2), "unit": "TFLOP/s", "ms": round(t * 1e3, 3),
             "attention_ms": round(t_attn * 1e3, 3),
             "roofline": {"bound": "tensor", "achieved": round(flops / t_attn / 1e12, 2),
-                         "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                         "frac": round(flops / t_attn / 1e12 / pk["bf16_sus"], 4)}}
+                         "peak": pk["bf16"], "unit": "TFLOP/s",
+                         "frac": round(flops / t_attn / 1e12 / pk["bf16"], 4)}}
         del ws
     res["value"], res["unit"] = res["bf16_pool"]["value"], "TFLOP/s"
     del inp
@@ -765,8 +768,8 @@ def bench_e4m3(msa, device, flush, seed=0, reps=3):
             "value": round(flops / t / 1e12, 2), "unit": "TFLOP/s", "ms": round(t * 1e3, 3),
             "attention_ms": round(t_attn * 1e3, 3),
             "roofline": {"bound": "tensor", "achieved": round(flops / t_attn / 1e12, 2),
-                         "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                         "frac": round(flops / t_attn / 1e12 / pk["bf16_sus"], 4)},
+                         "peak": pk["bf16"], "unit": "TFLOP/s",
+                         "frac": round(flops / t_attn / 1e12 / pk["bf16"], 4)},
             "executed_mma_tflops": round(flops_exec / t_attn / 1e12, 2)}
         del ws
     res["work_efficiency"] = round(flops / flops_exec, 4)

@@ -833,7 +833,11 @@ msa_status_t msa_proxy_score(const void* q, msa_dtype_t q_dtype, const void* k,
       (cu_seqlens_k && !aligned(cu_seqlens_k, 4)) || (page_table && !aligned(page_table, 4)) ||
       (seqused_k && !aligned(seqused_k, 4)))
     return MSA_INVALID_ARG;
-  if (head_dim != 128 || q_dtype != MSA_BF16 || k_dtype != MSA_BF16) return MSA_UNSUPPORTED;
+  // q bf16 or fp16; K of q's type, or E4M3 (upconverted to q's type in the kernel).
+  if (head_dim != 128 || (q_dtype != MSA_BF16 && q_dtype != MSA_FP16) ||
+      (k_dtype != q_dtype && k_dtype != MSA_FP8_E4M3))
+    return MSA_UNSUPPORTED;
+  const int k_esize = k_dtype == MSA_FP8_E4M3 ? 1 : 2;
   const int G = num_qo_heads / num_kv_heads;
   if (G > 128) return MSA_UNSUPPORTED;
   if (reduce_heads && (G > 32 || (G & (G - 1)) != 0)) return MSA_UNSUPPORTED;
@@ -843,9 +847,11 @@ msa_status_t msa_proxy_score(const void* q, msa_dtype_t q_dtype, const void* k,
   if (a.fault == nullptr) return MSA_CUDA_ERROR;
   const int Wm = tile_tokens_for(num_qo_heads, num_kv_heads);
   bool ok = map_rows(&a.tmap_q, q, 2, num_qo_heads, total_q, (uint32_t)G, (uint32_t)Wm);
-  ok = ok && (paged ? map_pages(&a.tmap_k, k, 2, num_kv_heads, num_pages)
-                    : map_rows(&a.tmap_k, k, 2, num_kv_heads, total_k, 1, 128));
+  ok = ok && (paged ? map_pages(&a.tmap_k, k, k_esize, num_kv_heads, num_pages)
+                    : map_rows(&a.tmap_k, k, k_esize, num_kv_heads, total_k, 1, 128));
   if (!ok) return MSA_CUDA_ERROR;
+  a.f16 = q_dtype == MSA_FP16 ? 1 : 0;
+  a.k_fp8 = k_esize == 1 ? 1 : 0;
   a.cu_q = cu_seqlens_q;
   a.cu_k = cu_seqlens_k;
   a.paged = paged ? 1 : 0;
@@ -869,8 +875,8 @@ msa_status_t msa_proxy_score(const void* q, msa_dtype_t q_dtype, const void* k,
   // Few tiles (decode-sized problems, under kProxyFewTiles per SM): split
   // each tile's block columns into slices so that there are about
   // kProxyCtasPerSM CTAs per SM, at least kProxyMinSlice columns each and at
-  // most what one pass over the groups holds (16384 / TQ columns).
-  const long long cap_cols = 16384 / TQ;
+  // most what one pass over the groups holds (the running-max buffer / TQ columns).
+  const long long cap_cols = (a.k_fp8 ? 14336 : 16384) / TQ;  // the kernel's running-max buffer
   long long sc = max_k_tiles;
   const long long target = (long long)kProxyCtasPerSM * kPlanSMs;
   if ((long long)a.max_tiles < (long long)kProxyFewTiles * kPlanSMs) {

@@ -323,6 +323,13 @@ MSA_DEV void e4m3x4_to_bf16(uint32_t w, uint32_t& lo, uint32_t& hi) {
   }
 }
 
+// Four E4M3 ("fn") codes, lowest byte first, to four f16 values (two packed
+// pairs), exactly (every E4M3 value is an f16 value).
+MSA_DEV void e4m3x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(lo) : "h"((uint16_t)(w & 0xffffu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hi) : "h"((uint16_t)(w >> 16)));
+}
+
 // Bytes of one (page, KV head) slice of packed NVFP4: 128 tokens x 64 bytes of
 // E2M1 pairs, and 128 x 8 E4M3 block scales (one per 16 elements).
 constexpr uint32_t kFp4Data = 128 * 64;

@@ -141,8 +141,9 @@ int device_smem_optin();
 
 struct ProxyArgs {
   unsigned* fault;      // device fault word (bounded-wait expiry, capacity)
-  CUtensorMap tmap_q;   // (d, Hq, Tq) bf16, box (64, G, Wm)
-  CUtensorMap tmap_k;   // flat (d, Hkv, Tk) / paged (d, 128, Hkv, pages) bf16, 128-key box
+  CUtensorMap tmap_q;   // (d, Hq, Tq) 16-bit, box (64, G, Wm)
+  CUtensorMap tmap_k;   // flat (d, Hkv, Tk) / paged (d, 128, Hkv, pages), 128-key box of
+                        // 128 bytes (64 16-bit values, or 128 E4M3 codes)
   const int32_t* cu_q;
   const int32_t* cu_k;        // flat lengths, or NULL when paged
   int paged;
@@ -163,6 +164,8 @@ struct ProxyArgs {
   int slice_cols;       // block columns per CTA: CTA (tile, s) takes [s, s + 1) * slice_cols
   int slices;           // column slices per tile
   float* out;
+  int f16;              // q (and 16-bit K) are fp16, else bf16
+  int k_fp8;            // K is E4M3, upconverted in the kernel to q's type
 };
 cudaError_t launch_proxy(const ProxyArgs& a, cudaStream_t s);
 

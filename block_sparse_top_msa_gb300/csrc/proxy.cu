@@ -18,6 +18,10 @@
 // (warp shuffles). With reduce_heads the running max over groups lives in
 // shared memory per (block, token) and is written once, coalesced, per block
 // column; the per-head buffer of the reference design is never materialised.
+// q and K are bf16 or fp16 (the MMA takes q's type); E4M3 K ("fn") is loaded
+// by TMA into a two-stage staging ring and upconverted exactly to q's type in
+// the MMA's swizzled layout by the eight epilogue warps, which convert block
+// t + 1 before taking the maxima of block t.
 #include <math.h>
 
 #include "common.cuh"
@@ -30,18 +34,22 @@ namespace {
 
 constexpr int kPxStages = 2;
 constexpr int kPxTile = 16384;
-constexpr int kPxRed = 16384;          // floats of running max (block column x token)
 constexpr int kPxEpiWarps = 8;
 constexpr int kPxProducerWarp = 8;
 constexpr int kPxMmaWarp = 9;
 constexpr int kPxThreads = 10 * 32;
 
+// F8K: an E4M3 staging ring, paid for with a smaller running-max buffer.
+template <bool F8K>
 struct __align__(1024) ProxySmem {
+  static constexpr int kRed = F8K ? 14336 : 16384;  // floats of running max (block column x token)
   uint8_t q[2][2][kPxTile];            // [M tile][d half]
   uint8_t k[kPxStages][2][kPxTile];
-  float red[kPxRed];                   // running max per (block column, token)
+  uint8_t k8[F8K ? kPxStages : 1][F8K ? kPxTile : 16];  // E4M3 K as loaded (F8K)
+  float red[kRed];                     // running max per (block column, token)
   uint64_t q_full, q_empty;
   uint64_t k_full[kPxStages], k_empty[kPxStages];
+  uint64_t f8_full[kPxStages], f8_empty[kPxStages];
   uint64_t s_full[2], s_free[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -49,13 +57,43 @@ struct __align__(1024) ProxySmem {
   int abort;
 };
 
+// One 128 x 128 E4M3 K tile (TMA SWIZZLE_128B image, 128-byte rows) to the
+// two 64-column 16-bit halves the MMA reads, by the 256 epilogue threads.
+template <bool F16>
+MSA_DEV void px_convert_tile(const uint8_t* src, uint8_t* dst_half0, int t) {
+#pragma unroll 2
+  for (int i = t; i < 1024; i += kPxEpiWarps * 32) {
+    const int r = i >> 3, c = i & 7;
+    const uint4 raw = *reinterpret_cast<const uint4*>(src + sw128_offset(r, c));
+    uint32_t w[8];
+    if (F16) {
+      e4m3x4_to_f16(raw.x, w[0], w[1]);
+      e4m3x4_to_f16(raw.y, w[2], w[3]);
+      e4m3x4_to_f16(raw.z, w[4], w[5]);
+      e4m3x4_to_f16(raw.w, w[6], w[7]);
+    } else {
+      e4m3x4_to_bf16(raw.x, w[0], w[1]);
+      e4m3x4_to_bf16(raw.y, w[2], w[3]);
+      e4m3x4_to_bf16(raw.z, w[4], w[5]);
+      e4m3x4_to_bf16(raw.w, w[6], w[7]);
+    }
+    uint8_t* dst = dst_half0 + (c >> 2) * kPxTile;
+    const int c16 = (c & 3) * 2;
+    *reinterpret_cast<uint4*>(dst + sw128_offset(r, c16)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(dst + sw128_offset(r, c16 + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
 // PAGED: K from a page pool. ONE_M: query tiles of Wm tokens, one M tile
 // (decode-sized calls, where no sequence has more than Wm query tokens).
-template <bool PAGED, bool ONE_M>
+// F8K: E4M3 K, upconverted by the epilogue warps.
+template <bool PAGED, bool ONE_M, bool F8K>
 __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_constant__ ProxyArgs a) {
   constexpr int MT = ONE_M ? 1 : 2;  // M tiles computed
+  using Smem = ProxySmem<F8K>;
+  constexpr int kPxRed = Smem::kRed;
   extern __shared__ uint8_t smem_raw[];
-  ProxySmem& sm = *reinterpret_cast<ProxySmem*>(
+  Smem& sm = *reinterpret_cast<Smem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   unsigned* fault = a.fault;
   volatile int* abort = &sm.abort;
@@ -96,8 +134,10 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
     mbar_init(&sm.q_full, 1);
     mbar_init(&sm.q_empty, 1);
     for (int s = 0; s < kPxStages; ++s) {
-      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_full[s], F8K ? kPxEpiWarps : 1);
       mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.f8_full[s], 1);
+      mbar_init(&sm.f8_empty[s], kPxEpiWarps);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.s_full[s], 1);
@@ -138,13 +178,28 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
         const int nc = chunk_cols(c);
         for (int j = 0; j < nc; ++j, ++it) {
           const int st = it % kPxStages;
+          // E4M3: the staging slot is free once its tile is converted; the
+          // converters themselves wait for the 16-bit slot.
+          uint64_t* free_bar = F8K ? &sm.f8_empty[st] : &sm.k_empty[st];
           if (it >= kPxStages &&
-              !mbar_wait(&sm.k_empty[st], ((it / kPxStages) - 1) & 1, fault, kFaultWaitMma,
-                         abort)) {
+              !mbar_wait(free_bar, ((it / kPxStages) - 1) & 1, fault,
+                         F8K ? kFaultWaitSoftmax : kFaultWaitMma, abort)) {
             ok = false;
             break;
           }
           const int t = c_lo + c * CH + j;
+          if (F8K) {
+            mbar_expect_tx(&sm.f8_full[st], kPxTile);
+            if (PAGED) {
+              int page = a.page_table[(size_t)b * a.max_pages + t];
+              if (page < 0 || page >= a.num_pages) page = a.num_pages;
+              tma_load_4d(sm.k8[st], &a.tmap_k, &sm.f8_full[st], 0, 0, g, page);
+            } else {
+              tma_load_3d(sm.k8[st], &a.tmap_k, &sm.f8_full[st], 0, g, kv0 + t * kBlk);
+            }
+            last_k[st] = it;
+            continue;
+          }
           mbar_expect_tx(&sm.k_full[st], 2 * kPxTile);
           if (PAGED) {
             int page = a.page_table[(size_t)b * a.max_pages + t];
@@ -161,12 +216,14 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
       }
       if (!ok) {
         for (int s = 0; s < kPxStages; ++s)
-          if (last_k[s] >= 0) mbar_wait(&sm.k_full[s], (last_k[s] / kPxStages) & 1, fault, kFaultWaitTma);
+          if (last_k[s] >= 0)
+            mbar_wait(F8K ? &sm.f8_full[s] : &sm.k_full[s], (last_k[s] / kPxStages) & 1, fault,
+                      kFaultWaitTma);
       }
     }
   } else if (warp == kPxMmaWarp) {
     if (lane == 0 && ncs > 0) {
-      const uint32_t idS = idesc_bf16_f32(128, 128, false, false);
+      const uint32_t idS = idesc_16bit_f32(128, 128, false, false, a.f16 != 0);
       int it = 0;
       bool ok = true;
       for (int p = 0; ok && p < nsteps; ++p) {
@@ -217,12 +274,36 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
     const uint32_t taddr_lane = tbase + ((uint32_t)(quad * 32) << 16);
     int it = 0;
     bool ok = true;
+    // E4M3: tile x (in the order the producer loads them) from staging slot
+    // x % 2 into 16-bit slot x % 2, once QK(x - 2) has released that slot.
+    const int ntiles = ncs * a.num_kv_heads;
+    auto convert = [&](int x) -> bool {
+      const int st = x % kPxStages;
+      bool okc = mbar_wait(&sm.f8_full[st], (x / kPxStages) & 1, fault, kFaultWaitTma, abort) &&
+                 (x < kPxStages ||
+                  mbar_wait(&sm.k_empty[st], ((x / kPxStages) - 1) & 1, fault, kFaultWaitMma, abort));
+      if (__any_sync(0xffffffffu, !okc)) return false;
+      if (a.f16) px_convert_tile<true>(sm.k8[st], sm.k[st][0], tid);
+      else px_convert_tile<false>(sm.k8[st], sm.k[st][0], tid);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&sm.f8_empty[st]);
+        mbar_arrive(&sm.k_full[st]);
+      }
+      return true;
+    };
+    if (F8K && ntiles > 0) ok = convert(0);
     for (int p = 0; ok && p < nsteps; ++p) {
       const int c = p / a.num_kv_heads, g = p % a.num_kv_heads;
       const int nc = chunk_cols(c);
       for (int j = 0; j < nc; ++j, ++it) {
         const int bb = it & 1;
         const int t = c_lo + c * CH + j;
+        if (F8K && it + 1 < ntiles && !convert(it + 1)) {
+          ok = false;
+          break;
+        }
         ok = mbar_wait(&sm.s_full[bb], (it >> 1) & 1, fault, kFaultWaitMma, abort);
         if (__any_sync(0xffffffffu, !ok)) {
           ok = false;
@@ -290,24 +371,29 @@ __global__ void __launch_bounds__(kPxThreads, 1) proxy_kernel(const __grid_const
   }
 }
 
-}  // namespace
-
-cudaError_t launch_proxy(const ProxyArgs& a, cudaStream_t s) {
-  const size_t smem = sizeof(ProxySmem) + 1024;
+template <bool F8K>
+cudaError_t launch_proxy_t(const ProxyArgs& a, cudaStream_t s) {
+  const size_t smem = sizeof(ProxySmem<F8K>) + 1024;
   cudaError_t e = cudaSuccess;
-  for (auto k : {proxy_kernel<false, false>, proxy_kernel<false, true>, proxy_kernel<true, false>,
-                 proxy_kernel<true, true>})
+  for (auto k : {proxy_kernel<false, false, F8K>, proxy_kernel<false, true, F8K>,
+                 proxy_kernel<true, false, F8K>, proxy_kernel<true, true, F8K>})
     if (e == cudaSuccess) e = set_smem_limit((const void*)k, (int)smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((long long)a.max_tiles * a.slices));
   if (a.paged) {
-    if (a.one_m) proxy_kernel<true, true><<<grid, kPxThreads, smem, s>>>(a);
-    else proxy_kernel<true, false><<<grid, kPxThreads, smem, s>>>(a);
+    if (a.one_m) proxy_kernel<true, true, F8K><<<grid, kPxThreads, smem, s>>>(a);
+    else proxy_kernel<true, false, F8K><<<grid, kPxThreads, smem, s>>>(a);
   } else {
-    if (a.one_m) proxy_kernel<false, true><<<grid, kPxThreads, smem, s>>>(a);
-    else proxy_kernel<false, false><<<grid, kPxThreads, smem, s>>>(a);
+    if (a.one_m) proxy_kernel<false, true, F8K><<<grid, kPxThreads, smem, s>>>(a);
+    else proxy_kernel<false, false, F8K><<<grid, kPxThreads, smem, s>>>(a);
   }
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_proxy(const ProxyArgs& a, cudaStream_t s) {
+  return a.k_fp8 ? launch_proxy_t<true>(a, s) : launch_proxy_t<false>(a, s);
 }
 
 }  // namespace msa

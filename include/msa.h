@@ -117,11 +117,14 @@ size_t msa_sparse_attention_workspace_size_kv(int batch, int total_q, int num_qo
  *                there), 256-byte aligned; its contents need no
  *                initialisation, and calls that share one workspace must be
  *                ordered on the device.
+ * Every route, decode-sized paged calls (seqlen_q <= 4) included, takes any
+ * G = Hq / Hkv up to 128: a query tile holds floor(128 / G) tokens (at least
+ * one), so a larger G only means fewer tokens per tile.
  * Returns MSA_INVALID_ARG when both or neither of cu_seqlens_k and page_table
  * are given (paged length comes only from seqused_k, per the page's rule of
  * declining two possibly disagreeing length sources), when Hq % Hkv != 0, or
  * when a pointer is NULL or misaligned; MSA_UNSUPPORTED for head_dim != 128,
- * a dtype pair other than those above, or topk outside [1, 64].
+ * G > 128, a dtype pair other than those above, or topk outside [1, 64].
  */
 msa_status_t msa_sparse_attention_fwd(
     const void* q, msa_dtype_t q_dtype, const void* k, const void* v, msa_dtype_t kv_dtype,
@@ -225,9 +228,11 @@ msa_status_t msa_sparse_attention_nvfp4_prepare(
  * reduce_heads != 0 the max is also taken over all query heads and the output
  * has one head.
  *
- *   q            device, (Tq, Hq, 128), MSA_BF16
- *   k            device, MSA_BF16; flat (Tk, Hkv, 128) when page_table is
- *                NULL, else a paged pool (num_pages, Hkv, 128, 128)
+ *   q            device, (Tq, Hq, 128), MSA_BF16 or MSA_FP16
+ *   k            device, q's dtype or MSA_FP8_E4M3 (E4M3 "fn", upconverted
+ *                exactly to q's type in the kernel); flat (Tk, Hkv, 128) when
+ *                page_table is NULL, else a paged pool (num_pages, Hkv, 128,
+ *                128) of k's element size
  *   cu_seqlens_q device int32 (B+1)
  *   cu_seqlens_k device int32 (B+1) for flat K; must be NULL when paged
  *   page_table   device int32 (B, max_pages) mapping batch-local block ->
@@ -244,8 +249,9 @@ msa_status_t msa_sparse_attention_nvfp4_prepare(
  * block columns across many CTAs; a block's max needs no merge.
  * Returns MSA_INVALID_ARG when both or neither of cu_seqlens_k and
  * page_table are given, when a paged call lacks seqused_k or max_pages, or as
- * for msa_sparse_attention_fwd; MSA_UNSUPPORTED for head_dim != 128, non-bf16
- * operands, or reduce_heads with G = Hq / Hkv not a power of two <= 32.
+ * for msa_sparse_attention_fwd; MSA_UNSUPPORTED for head_dim != 128, another
+ * dtype pair (e.g. bf16 q with fp16 K), or reduce_heads with G = Hq / Hkv not
+ * a power of two <= 32.
  */
 msa_status_t msa_proxy_score(const void* q, msa_dtype_t q_dtype, const void* k,
                              msa_dtype_t k_dtype, const int32_t* cu_seqlens_q,

@@ -263,6 +263,11 @@ def test_other_entry_point_errors(L):
                              128, 128, 1, 1, 1, vp(A), None) == 2  # reduce_heads, G = 48
     assert L.msa_proxy_score(vp(A), 0, vp(A), 0, vp(A), vp(A), None, 0, None, 1, 128, 128, 8, 2,
                              128, 128, 0, 1, 1, vp(A), None) == 1  # max_k_tiles 0
+    # proxy dtypes: q bf16 or fp16, K of q's type or E4M3; nothing else
+    BF16, FP16, E4M3 = 0, 1, 2
+    for qd, kd in ((BF16, FP16), (FP16, BF16), (E4M3, E4M3), (BF16, 9)):
+        assert L.msa_proxy_score(vp(A), qd, vp(A), kd, vp(A), vp(A), None, 0, None, 1, 128, 128,
+                                 8, 2, 128, 128, 1, 1, 1, vp(A), None) == 2, (qd, kd)
     # top-k
     assert L.msa_topk_select(vp(A), 3, 8, 16, 4, 2, vp(A), None) == 1   # heads 3 vs 2
     assert L.msa_topk_select(vp(A), 1, 8, 16, 65, 2, vp(A), None) == 2  # topk

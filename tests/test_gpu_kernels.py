@@ -307,6 +307,11 @@ DECODE_CASES = [
     ("sq8_g8", 8, [2500, 900, 260], 16, 2, 16),
     ("sq16_g16", 16, [5000], 32, 2, 16),
     ("sq32_g16", 32, [6000, 1000], 32, 2, 16),
+    # G above 16 on the decode route (any G up to 128 is accepted)
+    ("sq1_g32", 1, [9000, 300, 129, 4000], 64, 2, 16),
+    ("sq4_g32", 4, [7000, 260, 2000], 64, 2, 12),
+    ("sq2_g64", 2, [5000, 130, 3000], 128, 2, 8),
+    ("sq1_g128", 1, [4000, 700, 129], 128, 1, 16),
 ]
 
 

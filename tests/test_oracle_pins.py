@@ -527,3 +527,40 @@ def test_union_brute_force_and_invariants():
                     assert [union[j] for j in bits] == sorted(rowsets[w])
             tau += 1
     assert tau == ulen.shape[1]
+
+
+def test_proxy_e4m3_and_fp16_equal_bf16_on_shared_values():
+    """The proxy with E4M3 index-K, or with fp16 q and K, gives bit-identical
+    oracle scores to bf16 inputs holding the same values ("flashinfer.msa_ops.
+    msa_proxy_score", Parameters q (bf16 or fp16) and k (E4M3 upconverted)):
+    E4M3 K values are exact in bf16 and fp16, and k/16 with |k| < 256 is exact
+    in both 16-bit formats. Flat and paged, per head and reduced over heads."""
+    g = torch.Generator().manual_seed(21)
+    lens_q, lens_k = [3, 260], [700, 260]
+    Hq, Hkv, d = 8, 2, 128
+    cu_q = workloads.cu_from_lengths(lens_q)
+    cu_k = workloads.cu_from_lengths(lens_k)
+    su = torch.tensor(lens_k, dtype=torch.int32)
+    q = torch.randn(sum(lens_q), Hq, d, generator=g).to(torch.bfloat16)
+    k8 = torch.randn(sum(lens_k), Hkv, d, generator=g).to(torch.float8_e4m3fn)
+    k8p, pt = _to_paged(k8.view(torch.uint8), lens_k, Hkv, d, torch.Generator().manual_seed(4))
+    k8p = k8p.view(torch.float8_e4m3fn)
+    kbp = k8p.to(torch.bfloat16)
+    qs = (torch.randint(-255, 256, (sum(lens_q), Hq, d), generator=g).double() / 16.0)
+    ks = (torch.randint(-255, 256, (sum(lens_k), Hkv, d), generator=g).double() / 16.0)
+    for red in (False, True):
+        kw = dict(causal=True, max_k_tiles=6, reduce_heads=red)
+        e8 = oracle.proxy_score(q, k8, cu_q, cu_k, **kw)
+        eb = oracle.proxy_score(q, k8.to(torch.bfloat16), cu_q, cu_k, **kw)
+        np.testing.assert_array_equal(e8, eb)
+        p8 = oracle.proxy_score(q, k8p, cu_q, None, page_table=pt, seqused_k=su, **kw)
+        pb = oracle.proxy_score(q, kbp, cu_q, None, page_table=pt, seqused_k=su, **kw)
+        np.testing.assert_array_equal(p8, pb)
+        np.testing.assert_array_equal(p8, e8)
+        fh = oracle.proxy_score(qs.half(), ks.half(), cu_q, cu_k, **kw)
+        fb = oracle.proxy_score(qs.bfloat16(), ks.bfloat16(), cu_q, cu_k, **kw)
+        np.testing.assert_array_equal(fh, fb)
+        h8 = oracle.proxy_score(q.half(), k8, cu_q, cu_k, **kw)
+        hh = oracle.proxy_score(q.half(), k8.half(), cu_q, cu_k, **kw)
+        np.testing.assert_array_equal(h8, hh)
+        assert np.isfinite(e8[..., 3:]).any()
