@@ -86,7 +86,7 @@ def barrier(world):
 # of the build that was captured; otherwise the roofline's "traffic" is null.
 TRAFFIC_SOURCES = ("prefill.cu", "common.cuh", "tmem_wide.cuh", "internal.h", "tmap.h", "api.cu",
                    "union.cu", "tile_map.cuh")
-TRAFFIC_MEASURED = {"fingerprint": "0c3bc5ae389f0474", "bytes_per_launch": 2.427e9,
+TRAFFIC_MEASURED = {"fingerprint": "deb81fccf1c4bc6d", "bytes_per_launch": 2.4284e9,
                     "profile": "profiles/prefill_kernel_flat_varlen_2x32768_traffic.md"}
 
 
@@ -260,6 +260,107 @@ def cpu_baseline_prefill(inp, rows_target=3072, threads=None):
                             softmax_scale=scale, rows=rows, threads=cores)
     dt = time.perf_counter() - t0
     return flops / dt / 1e12, cores, f"{len(rows)} of {tq} query rows x all {cpu['q'].shape[1]} heads", dt
+
+
+def _oracle_attention_s(inp, rows, threads, paged=False):
+    """Seconds of one oracle sparse_attention call over `rows` (all rows when None)."""
+    import oracle
+    kw = dict(causal=True, softmax_scale=float(np.float32(inp.get("softmax_scale", D ** -0.5))),
+              rows=rows, threads=threads)
+    if paged:
+        kw.update(page_table=inp["page_table"], seqused_k=inp["seqused_k"])
+    t0 = time.perf_counter()
+    oracle.sparse_attention(inp["q"], inp["k"], inp["v"], inp["q2k_indices"],
+                            inp["cu_seqlens_q"], inp.get("cu_seqlens_k"), **kw)
+    return time.perf_counter() - t0
+
+
+def _attn_flops(inp, rows, k_lens):
+    hkv = inp["k"].shape[1]
+    G = inp["q"].shape[1] // hkv
+    cnt = visible_counts(inp["q2k_indices"], inp["cu_seqlens_q"], k_lens)
+    return 4.0 * D * G * float(cnt.sum() if rows is None else cnt[:, rows.long()].sum())
+
+
+def _row_sample(tq, n, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.sort(torch.randperm(tq, generator=g)[:n])[0].to(torch.int32)
+
+
+def cpu_baseline_suite(device, cores, inp2):
+    """The oracle on the other workloads and on one thread: the tiny flat
+    prefill and the paged decode in full; the mixed E4M3 prefill and the
+    two-stage pipeline on row samples, with the full-workload time
+    extrapolated by work (visible keys, or causal key counts for the proxy)
+    and marked so; the flat varlen prefill on one thread (a row sample)."""
+    import oracle
+    res = {}
+    # flat varlen prefill, one thread
+    rows = _row_sample(inp2["q"].shape[0], 128, 11)
+    dt = _oracle_attention_s(inp2, rows, 1)
+    res["one_thread"] = {"workload": workloads.FLAT_VARLEN.name, "threads": 1,
+                         "sample": "128 query rows x all heads",
+                         "tflops": _attn_flops(inp2, rows, inp2["lengths"]) / dt / 1e12,
+                         "seconds": round(dt, 3)}
+    # tiny flat prefill, in full
+    inp = workloads.make_prefill(workloads.TINY_FLAT, 0, device="cpu")
+    dt = _oracle_attention_s(inp, None, cores)
+    res["tiny_flat"] = {"workload": workloads.TINY_FLAT.name, "sample": "full",
+                        "tflops": _attn_flops(inp, None, inp["lengths"]) / dt / 1e12,
+                        "seconds": round(dt, 3)}
+    # paged decode, in full (s_q 1 and 4)
+    for sq in (1, 4):
+        inp = workloads.make_decode(workloads.PAGED_DECODE, 0, device="cpu", seqlen_q=sq)
+        su = inp["seqused_k"].tolist()
+        dt = _oracle_attention_s(inp, None, cores, paged=True)
+        res[f"paged_decode_sq{sq}"] = {
+            "workload": workloads.PAGED_DECODE.name, "seqlen_q": sq, "sample": "full",
+            "tflops": _attn_flops(inp, None, su) / dt / 1e12, "seconds": round(dt, 3)}
+        del inp
+    # mixed E4M3 prefill: row sample, extrapolated
+    inp = workloads.make_prefill(workloads.MIXED_E4M3, 0, device=device)
+    inp = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    tq = inp["q"].shape[0]
+    rows = _row_sample(tq, 512, 12)
+    dt = _oracle_attention_s(inp, rows, cores)
+    f_s, f_all = _attn_flops(inp, rows, inp["lengths"]), _attn_flops(inp, None, inp["lengths"])
+    res["mixed_e4m3"] = {"workload": workloads.MIXED_E4M3.name,
+                         "sample": f"512 of {tq} query rows x all heads",
+                         "tflops": f_s / dt / 1e12, "seconds": round(dt, 3),
+                         "full_seconds_extrapolated": round(dt * f_all / f_s, 1),
+                         "extrapolated": True}
+    del inp
+    # two-stage: proxy scores, top-k and attention for a row sample
+    spec = workloads.TWO_STAGE
+    inp = workloads.make_two_stage(spec, 0, device=device)
+    inp = {k: (v.cpu() if torch.is_tensor(v) else v) for k, v in inp.items()}
+    L = spec.seqlens[0]
+    T = (L + 127) // 128
+    rows = _row_sample(L, 64, 13)
+    t0 = time.perf_counter()
+    sc = oracle.proxy_score(inp["proxy_q"], inp["index_k"], inp["cu_seqlens_q"],
+                            inp["cu_seqlens_k"], causal=True, max_k_tiles=T, reduce_heads=True,
+                            rows=rows, threads=cores)
+    t_proxy = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    sel = oracle.topk_select(np.ascontiguousarray(sc.astype(np.float32)), spec.topk,
+                             spec.num_kv_heads)
+    t_topk = time.perf_counter() - t0
+    q2k = torch.full((spec.num_kv_heads, L, spec.topk), -1, dtype=torch.int32)
+    q2k[:, rows.long()] = torch.as_tensor(np.asarray(sel), dtype=torch.int32)
+    inp["q2k_indices"] = q2k
+    t_attn = _oracle_attention_s(inp, rows, cores)
+    keys_s = float((rows.long() + 1).sum())  # causal keys of the sampled rows
+    keys_all = L * (L + 1) / 2
+    f_s = _attn_flops(inp, rows, [L])
+    res["two_stage"] = {
+        "workload": spec.name, "sample": f"64 of {L} query rows (proxy over all heads, top-k, "
+        "attention)", "seconds": round(t_proxy + t_topk + t_attn, 3),
+        "proxy_tflops": 2.0 * D * spec.proxy_heads * keys_s / t_proxy / 1e12,
+        "attention_tflops": f_s / t_attn / 1e12,
+        "full_seconds_extrapolated": round(t_proxy * keys_all / keys_s + t_attn * L / len(rows), 1),
+        "extrapolated": True}
+    return res
 
 
 def bench_prefill(msa, args, device, world, rank):
@@ -914,6 +1015,11 @@ def main():
         v, cores, sample, dt = cpu_baseline_prefill(inp_cpu)
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": sample, "seconds": round(dt, 2)}
+        if not args.no_secondary:
+            inp2 = {k: (t.cpu() if torch.is_tensor(t) else t) for k, t in inp_cpu.items()}
+            del inp_cpu
+            torch.cuda.empty_cache()
+            cpu["other"] = cpu_baseline_suite(device, cpu["cores"], inp2)
     if rank == 0:
         spec = res["spec"]
         line = {
