@@ -88,10 +88,12 @@ struct PrefillArgs {
   int max_tiles;
   int cap;
   int words;
-  const int32_t* union_len;
-  const int32_t* union_blocks;
+  // Union metadata (written by the union kernel, or in direct mode by this
+  // kernel's item setup).
+  int32_t* union_len;
+  int32_t* union_blocks;
   const uint32_t* member;
-  const int32_t* tile_info;
+  int32_t* tile_info;
   void* out;
   float* lse;
   // Work items, handed out dynamically to a persistent grid. Units are (query tile, KV head)

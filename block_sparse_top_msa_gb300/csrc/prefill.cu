@@ -409,14 +409,14 @@ MSA_DEV Item direct_item(const PrefillArgs& a, int i) {
   }
   // The union arrays are indexed (KV head, tile), like the union kernel's.
   const size_t slot = (size_t)it.h * a.max_tiles + it.tile;
-  int32_t* dst = const_cast<int32_t*>(a.union_blocks) + slot * a.cap;
+  int32_t* dst = a.union_blocks + slot * a.cap;
   int n = 0;
 #pragma unroll
   for (int j = 0; j < kN; ++j) {
     if (key[j] != INT_MAX && (j == 0 || key[j] != key[j - 1])) dst[n++] = key[j];
   }
-  const_cast<int32_t*>(a.union_len)[slot] = n;
-  int32_t* ti = const_cast<int32_t*>(a.tile_info) + 2 * it.tile;
+  a.union_len[slot] = n;
+  int32_t* ti = a.tile_info + 2 * it.tile;
   ti[0] = it.t0;
   ti[1] = it.b;
   it.n_union = n;
