@@ -453,6 +453,9 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
   static_assert(!(FP8 && F16), "E4M3 K/V are upconverted to bf16");
   using R = Roles<FP8>;
   using Smem = PrefillSmem<FP8, STREAM>;
+  // 16-bit prefill layout (long items): an item's epilogue is deferred until
+  // the next item's first block has published its P.
+  constexpr bool kDeferEpilogue = !STREAM && !FP8;
   constexpr int kQBuf = Smem::kQBuf;
   constexpr int kKStages = Smem::kKStages;
   constexpr int kVStages = Smem::kVStages;
@@ -914,6 +917,86 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
       ++xi;
       return slot[(1 - wg) * 128 + row];
     };
+    // Item epilogue: out = O / l and the natural-log LSE (or the fp32
+    // partials of a split item). It is deferred until the next item's first
+    // block has published its P, so that the next item's first PV (which
+    // overwrites O) waits only for O to be read, not for a whole softmax
+    // pass as well.
+    struct Epi {
+      bool valid;
+      int glast, tail, split, nsplit;
+      float m_ref, l;
+      bool active;
+      size_t orow;
+    };
+    Epi pe{};
+    pe.valid = false;
+    constexpr bool kDefer = kDeferEpilogue;
+    auto run_epilogue = [&](const Epi& e) -> bool {
+      bool okk = pv_wait(e.glast);
+      okk = !__any_sync(0xffffffffu, !okk);
+      float lt = e.l;  // the row's full sum
+      if constexpr (NW == 2) lt += exchange(e.l, okk);
+      if (!okk) return false;
+      tc_fence_after();
+      const size_t part = ((size_t)(e.tail < 0 ? 0 : e.tail) * a.splits + e.split) * a.rows_part;
+      const bool has = lt > 0.f;
+      const float os = a.out_scale;  // output scale (the NVFP4 V global scale; else 1)
+      const float inv = has ? os / lt : 0.f;
+      auto store_half = [&](int half, const float* o) {
+        if (!e.active) return;
+        if (e.nsplit == 1) {
+          uint4* dst =
+              reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + e.orow * 128);
+#pragma unroll
+          for (int c = 0; c < 64; c += 8) {
+            uint4 v4 = make_uint4(0u, 0u, 0u, 0u);
+            if (has)
+              v4 = make_uint4(pack_x2<F16>(o[c] * inv, o[c + 1] * inv),
+                              pack_x2<F16>(o[c + 2] * inv, o[c + 3] * inv),
+                              pack_x2<F16>(o[c + 4] * inv, o[c + 5] * inv),
+                              pack_x2<F16>(o[c + 6] * inv, o[c + 7] * inv));
+            dst[(half * 64 + c) >> 3] = v4;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(a.part_o + (part + row) * 128 + half * 64);
+#pragma unroll
+          for (int c = 0; c < 64; c += 4)
+            dst[c >> 2] = make_float4(o[c] * os, o[c + 1] * os, o[c + 2] * os, o[c + 3] * os);
+        }
+      };
+      // O is released (the next item's first PV may overwrite it) as soon as
+      // this warp's columns are in registers, before the global stores.
+      {
+        float o[64];
+        tmem_ld64(lane_base + kColO + wg * kHalves * 64, o);
+        if (kHalves == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.o_free);
+        }
+        store_half(wg * kHalves, o);
+      }
+      if (kHalves == 2) {
+        float o[64];
+        tmem_ld64(lane_base + kColO + 64, o);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.o_free);
+        store_half(1, o);
+      }
+      if (e.nsplit == 1) {
+        if (e.active && wg == 0 && a.lse != nullptr)
+          a.lse[e.orow] = has ? (e.m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+        return true;
+      }
+      if (e.active && wg == 0) {
+        a.part_ml[(part + row) * 2] = e.m_ref;
+        a.part_ml[(part + row) * 2 + 1] = lt;
+      }
+      // The unit's splits are combined by merge_splits_kernel after this launch.
+      return true;
+    };
     // Both warps of a pair agree on each read's outcome before going on
     // (they meet at paired barriers below).
     for (int ni = 0;; ++ni) {
@@ -1071,74 +1154,97 @@ __global__ void __launch_bounds__(Roles<FP8>::kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.p_full[bb]);
+        if (kDefer && u == 0 && pe.valid) {
+          ok = run_epilogue(pe);
+          pe.valid = false;
+          if (!ok) break;
+        }
       }
       if (!ok) break;
-      // ---------------------------------------------------- item epilogue
-      const int glast = g + it.n - 1;
-      ok = pv_wait(glast);
-      ok = !__any_sync(0xffffffffu, !ok);
-      float lt = l;  // the row's full sum
-      if constexpr (NW == 2) lt += exchange(l, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const size_t part = ((size_t)(it.tail < 0 ? 0 : it.tail) * a.splits + it.split) * a.rows_part;
-      const bool has = lt > 0.f;
-      const float os = a.out_scale;  // output scale (the NVFP4 V global scale; else 1)
-      const float inv = has ? os / lt : 0.f;
-      auto store_half = [&](int half, const float* o) {
-        if (!active) return;
-        if (nsplit == 1) {
-          uint4* dst =
-              reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * 128);
-#pragma unroll
-          for (int c = 0; c < 64; c += 8) {
-            uint4 v4 = make_uint4(0u, 0u, 0u, 0u);
-            if (has)
-              v4 = make_uint4(pack_x2<F16>(o[c] * inv, o[c + 1] * inv),
-                              pack_x2<F16>(o[c + 2] * inv, o[c + 3] * inv),
-                              pack_x2<F16>(o[c + 4] * inv, o[c + 5] * inv),
-                              pack_x2<F16>(o[c + 6] * inv, o[c + 7] * inv));
-            dst[(half * 64 + c) >> 3] = v4;
+      if constexpr (kDefer) {
+        // This item's epilogue runs once the next item's first block has
+        // published its P (or after the last item).
+        pe.valid = true;
+        pe.glast = g + it.n - 1;
+        pe.tail = it.tail;
+        pe.split = it.split;
+        pe.nsplit = nsplit;
+        pe.m_ref = m_ref;
+        pe.l = l;
+        pe.active = active;
+        pe.orow = orow;
+        g += it.n;
+      } else {
+        // Decode layout: the epilogue in line at the item's end (the same
+        // work as run_epilogue; the deferred form measured slower there).
+        // ---------------------------------------------------- item epilogue
+        const int glast = g + it.n - 1;
+        ok = pv_wait(glast);
+        ok = !__any_sync(0xffffffffu, !ok);
+        float lt = l;  // the row's full sum
+        if constexpr (NW == 2) lt += exchange(l, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const size_t part = ((size_t)(it.tail < 0 ? 0 : it.tail) * a.splits + it.split) * a.rows_part;
+        const bool has = lt > 0.f;
+        const float os = a.out_scale;  // output scale (the NVFP4 V global scale; else 1)
+        const float inv = has ? os / lt : 0.f;
+        auto store_half = [&](int half, const float* o) {
+          if (!active) return;
+          if (nsplit == 1) {
+            uint4* dst =
+                reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.out) + orow * 128);
+  #pragma unroll
+            for (int c = 0; c < 64; c += 8) {
+              uint4 v4 = make_uint4(0u, 0u, 0u, 0u);
+              if (has)
+                v4 = make_uint4(pack_x2<F16>(o[c] * inv, o[c + 1] * inv),
+                                pack_x2<F16>(o[c + 2] * inv, o[c + 3] * inv),
+                                pack_x2<F16>(o[c + 4] * inv, o[c + 5] * inv),
+                                pack_x2<F16>(o[c + 6] * inv, o[c + 7] * inv));
+              dst[(half * 64 + c) >> 3] = v4;
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(a.part_o + (part + row) * 128 + half * 64);
+  #pragma unroll
+            for (int c = 0; c < 64; c += 4)
+              dst[c >> 2] = make_float4(o[c] * os, o[c + 1] * os, o[c + 2] * os, o[c + 3] * os);
           }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + (part + row) * 128 + half * 64);
-#pragma unroll
-          for (int c = 0; c < 64; c += 4)
-            dst[c >> 2] = make_float4(o[c] * os, o[c + 1] * os, o[c + 2] * os, o[c + 3] * os);
+        };
+        // O is released (the next item's first PV may overwrite it) as soon as
+        // this warp's columns are in registers, before the global stores.
+        {
+          float o[64];
+          tmem_ld64(lane_base + kColO + wg * kHalves * 64, o);
+          if (kHalves == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.o_free);
+          }
+          store_half(wg * kHalves, o);
         }
-      };
-      // O is released (the next item's first PV may overwrite it) as soon as
-      // this warp's columns are in registers, before the global stores.
-      {
-        float o[64];
-        tmem_ld64(lane_base + kColO + wg * kHalves * 64, o);
-        if (kHalves == 1) {
+        if (kHalves == 2) {
+          float o[64];
+          tmem_ld64(lane_base + kColO + 64, o);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sm.o_free);
+          store_half(1, o);
         }
-        store_half(wg * kHalves, o);
+        g += it.n;
+        if (nsplit == 1) {
+          if (active && wg == 0 && a.lse != nullptr)
+            a.lse[orow] = has ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+          continue;
+        }
+        if (active && wg == 0) {
+          a.part_ml[(part + row) * 2] = m_ref;
+          a.part_ml[(part + row) * 2 + 1] = lt;
+        }
+        // The unit's splits are combined by merge_splits_kernel after this launch.
       }
-      if (kHalves == 2) {
-        float o[64];
-        tmem_ld64(lane_base + kColO + 64, o);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.o_free);
-        store_half(1, o);
-      }
-      g += it.n;
-      if (nsplit == 1) {
-        if (active && wg == 0 && a.lse != nullptr)
-          a.lse[orow] = has ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
-        continue;
-      }
-      if (active && wg == 0) {
-        a.part_ml[(part + row) * 2] = m_ref;
-        a.part_ml[(part + row) * 2 + 1] = lt;
-      }
-      // The unit's splits are combined by merge_splits_kernel after this launch.
     }
+    if (kDefer && ok && pe.valid) ok = run_epilogue(pe);
   }
 
   tc_fence_before();
