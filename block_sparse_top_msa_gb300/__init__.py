@@ -8,7 +8,8 @@ if the library has not been built, every call raises.
 
 Convenience defaults that need information the C ABI takes explicitly
 (``max_seqlen_q``, ``max_k_tiles``) are derived here from ``cu_seqlens`` /
-``seqused_k`` when omitted. That derivation READS THE DEVICE: a
+``seqused_k`` when omitted. That derivation READS THE DEVICE (except
+``max_seqlen_q`` of a single sequence, which is ``total_q``): a
 device-to-host copy that synchronises the host with the GPU and launches
 two small torch kernels on every such call. Code that must not synchronise
 (CUDA-graph capture, pipelined serving loops) passes them explicitly; the C
@@ -159,6 +160,12 @@ def _max_len(cu: torch.Tensor) -> int:
     return int((cu[1:] - cu[:-1]).max().item()) if cu.numel() > 1 else 0
 
 
+def _q_bound(cu_q: torch.Tensor, total_q: int) -> int:
+    """A bound on every query run: total_q itself for one sequence (no device
+    read), else the longest run read back from the device (a host sync)."""
+    return total_q if cu_q.numel() == 2 else _max_len(cu_q)
+
+
 def msa_union_tile_tokens(num_qo_heads: int, num_kv_heads: int) -> int:
     return int(lib().msa_union_tile_tokens(num_qo_heads, num_kv_heads))
 
@@ -206,9 +213,11 @@ def msa_sparse_attention_fwd(q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k=No
                              workspace=None, stream=None):
     """Sparse attention forward; see ``msa_sparse_attention_fwd`` in include/msa.h.
 
-    Returns ``out`` or ``(out, lse)``. With ``max_seqlen_q=None`` the longest
-    query run is read back from ``cu_seqlens_q`` on the device, which
-    synchronises the host; pass it to keep the call asynchronous.
+    Returns ``out`` or ``(out, lse)``. With ``max_seqlen_q=None`` and more
+    than one sequence the longest query run is read back from
+    ``cu_seqlens_q`` on the device, which synchronises the host; pass it to
+    keep the call asynchronous (one sequence needs no read: its run is
+    ``total_q``).
     """
     L = lib()
     args, out, lse, workspace = _forward_args(
@@ -237,7 +246,7 @@ def _forward_args(q, k, v, q2k_indices, cu_seqlens_q, cu_seqlens_k, causal, soft
     batch = cu_seqlens_q.shape[0] - 1
     paged = page_table is not None
     if max_seqlen_q is None:
-        max_seqlen_q = _max_len(cu_seqlens_q)
+        max_seqlen_q = _q_bound(cu_seqlens_q, total_q)
     if out is None:
         out = torch.empty_like(q)
     if lse is None and return_softmax_lse:
@@ -329,7 +338,7 @@ def _fp4_args(q, k, k_scale, v, v_scale, q2k_indices, cu_seqlens_q, page_table, 
     hkv, topk = k.shape[1], q2k_indices.shape[2]
     batch = cu_seqlens_q.shape[0] - 1
     if max_seqlen_q is None:
-        max_seqlen_q = _max_len(cu_seqlens_q)
+        max_seqlen_q = _q_bound(cu_seqlens_q, total_q)
     if out is None:
         out = torch.empty_like(q)
     if lse is None and return_softmax_lse:
