@@ -822,6 +822,46 @@ def bench_two_stage(msa, device, flush, seed=0):
     return res
 
 
+# ---------------------------------------------------------------- secondary: tiny flat prefill
+def bench_tiny(msa, device, flush, seed=0, reps=20):
+    """The tiny flat prefill (1 x 1024 tokens, 4/1 heads, top-4): a
+    latency-bound call (32 query tiles of 32 tokens for one KV head, far
+    fewer work items than SMs); the whole call (union and attention kernels)
+    by events around it, the L2 flushed before each."""
+    spec = workloads.TINY_FLAT
+    inp = workloads.make_prefill(spec, seed, device=device)
+    tq, hq, _ = inp["q"].shape
+    hkv = inp["k"].shape[1]
+    flops = 4.0 * D * (hq // hkv) * float(
+        visible_counts(inp["q2k_indices"], inp["cu_seqlens_q"], inp["lengths"]).sum())
+    max_sq = max(inp["lengths"])
+    need = msa.msa_sparse_attention_workspace_size(len(inp["lengths"]), tq, hq, hkv, D, spec.topk,
+                                                   max_sq, False)
+    ws = torch.empty(need, dtype=torch.uint8, device=device)
+    out = torch.empty_like(inp["q"])
+    lse = torch.empty((tq, hq), dtype=torch.float32, device=device)
+
+    def call():
+        run_prefill(msa, inp, out, lse, ws, max_sq)
+
+    for _ in range(3):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ts = []
+    for _ in range(reps):
+        flush.fill_(1)
+        torch.cuda._sleep(200_000)  # keeps the GPU busy while the host enqueues the call
+        e0.record()
+        call()
+        e1.record()
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1) * 1e-3)
+    t = statistics.median(ts)
+    return {"workload": spec.name, "tflops": round(flops / t / 1e12, 3), "us": round(t * 1e6, 2),
+            "algorithmic_gflop": round(flops / 1e9, 3),
+            "roofline": {"bound": "latency", "note": "32 work items on a 152-SM GPU"}}
+
+
 # ---------------------------------------------------------------- secondary: E4M3 K/V prefill
 def bench_e4m3(msa, device, flush, seed=0, reps=3):
     """Flat varlen prefill with E4M3 K/V, bf16 q, on both routes: the default
@@ -1007,6 +1047,8 @@ def main():
         secondary["two_stage"] = bench_two_stage(msa, device, flush)
         torch.cuda.empty_cache()
         secondary["e4m3_prefill"] = bench_e4m3(msa, device, flush)
+        torch.cuda.empty_cache()
+        secondary["tiny_prefill"] = bench_tiny(msa, device, flush)
     else:
         res.pop("inp")
     cpu = None
