@@ -97,6 +97,37 @@ def test_proxy_dtypes_paged_e4m3(msa, case):
     check_proxy(got, ref, label=name)
 
 
+@pytest.mark.parametrize("sq", [1, None])
+def test_proxy_f16_paged(msa, sq):
+    """fp16 q with an fp16 paged K pool, decode-shaped (one query token per
+    request, column slices) and prefill-shaped, with an unmapped page."""
+    g = torch.Generator().manual_seed(900 + (sq or 0))
+    seqused = [4000, 700, 129]
+    lens_q = list(seqused) if sq is None else [sq] * len(seqused)
+    cu_q = workloads.cu_from_lengths(lens_q)
+    pages = [(n + 127) // 128 for n in seqused]
+    npg = sum(pages) + 2
+    perm = torch.randperm(npg, generator=g).to(torch.int32)
+    pt = torch.zeros(len(seqused), max(pages), dtype=torch.int32)
+    off = 0
+    for b, n in enumerate(pages):
+        pt[b, :n] = perm[off:off + n]
+        off += n
+    pt[1, 1] = npg + 3
+    k = torch.randn(npg, 2, 128, 128, generator=g).to(torch.float16)
+    q = torch.randn(sum(lens_q), 16, 128, generator=g).to(torch.float16)
+    su = torch.tensor(seqused, dtype=torch.int32)
+    T = max(pages) + 1
+    got = msa.msa_proxy_score(q.to(DEV), k.to(DEV), cu_q.to(DEV), None, causal=True,
+                              max_k_tiles=T, reduce_heads=True, page_table=pt.to(DEV),
+                              seqused_k=su.to(DEV), max_seqlen_q=sq)
+    torch.cuda.synchronize()
+    fault_clear(msa)
+    ref = oracle.proxy_score(q, k, cu_q, None, page_table=pt, seqused_k=su, causal=True,
+                             max_k_tiles=T, reduce_heads=True)
+    check_proxy(got, ref, label=f"f16_paged_sq{sq}")
+
+
 def test_proxy_e4m3_equals_bf16_copy(msa):
     """The in-kernel upconversion gives exactly the scores of the same K
     converted to bf16 beforehand (E4M3 is exact in bf16): bit-identical."""
