@@ -35,6 +35,9 @@ unsigned* fault_word() {
 namespace {
 
 constexpr int kMaxTopk = 64;
+// Packed-NVFP4 calls with at most this many query tokens per request (and
+// G <= 16) take the decode kernel.
+constexpr int kFp4DecodeMaxSeqQ = 16;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -250,6 +253,16 @@ bool map_pages(CUtensorMap* m, const void* base, int esize, int H, int pages) {
                       4, base, dims, strides, box);
 }
 
+// (64 bytes, 128, H, pages) map over the packed-NVFP4 code slices of a planar
+// page pool (slice (p, h) at p * page_stride + h * 8192), 64-byte swizzle.
+bool map_fp4_codes(CUtensorMap* m, const void* base, int H, int pages, long long page_stride) {
+  const uint64_t dims[4] = {64, 128, (uint64_t)H, (uint64_t)pages};
+  const uint64_t strides[3] = {64, 64ull * 128, (uint64_t)page_stride};
+  const uint32_t box[4] = {64u, 128u, 1u, 1u};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 msa_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MSA_OK : MSA_CUDA_ERROR; }
 
 cudaEvent_t g_timing[3] = {nullptr, nullptr, nullptr};
@@ -372,6 +385,8 @@ struct ForwardPlan {
   PrefillArgs a{};
   bool swapped = false;  // the swapped-orientation prefill kernel, else the union-tile kernel
   bool skip_union = false;  // direct mode: the attention kernel builds one-token unions itself
+  bool fp4_decode = false;  // packed-NVFP4 decode-shaped call: fp4_decode_kernel alone
+  Fp4DecodeArgs f4{};
 };
 
 // The swapped-kernel part of a forward plan (arguments already checked).
@@ -691,12 +706,49 @@ msa_status_t build_forward_fp4(
   a.fp4_page_stride = page_stride;
   a.scale_log2 *= k_global_scale;
   a.out_scale = v_global_scale;
+  // Decode-shaped calls (G <= 16, a few query tokens per request): one unit
+  // per (token, KV head) in the register-dequantizing decode kernel.
+  const int G = num_qo_heads / num_kv_heads;
+  if (G <= 16 && max_seqlen_q <= kFp4DecodeMaxSeqQ) {
+    Fp4DecodeArgs& f = plan->f4;
+    if (!map_fp4_codes(&f.tmap_kc, k, num_kv_heads, num_pages, page_stride) ||
+        !map_fp4_codes(&f.tmap_vc, v, num_kv_heads, num_pages, page_stride))
+      return MSA_CUDA_ERROR;
+    f.fault = a.fault;
+    f.q = static_cast<const uint16_t*>(q);
+    f.q2k = q2k_indices;
+    f.topk = topk;
+    f.cu_q = cu_seqlens_q;
+    f.page_table = page_table;
+    f.max_pages = max_pages;
+    f.num_pages = num_pages;
+    f.seqused_k = seqused_k;
+    f.k_scale = static_cast<const uint8_t*>(k_scale);
+    f.v_scale = static_cast<const uint8_t*>(v_scale);
+    f.page_stride = page_stride;
+    f.batch = batch;
+    f.total_q = total_q;
+    f.num_qo_heads = num_qo_heads;
+    f.num_kv_heads = num_kv_heads;
+    f.G = G;
+    f.scale_log2 = a.scale_log2;
+    f.out_scale = v_global_scale;
+    f.out = static_cast<uint16_t*>(out);
+    f.lse = lse;
+    plan->fp4_decode = true;
+  }
   return MSA_OK;
 }
 
 msa_status_t launch_forward(const ForwardPlan& p, cudaStream_t stream) {
   if (p.empty) return MSA_OK;
   mark(0, stream);
+  if (p.fp4_decode) {
+    mark(1, stream);
+    const cudaError_t e = launch_fp4_decode(p.f4, stream);
+    mark(2, stream);
+    return from_cuda(e);
+  }
   cudaError_t e = launch_kv_decode(p.dq, stream);
   if (e != cudaSuccess) return MSA_CUDA_ERROR;
   e = launch_page_decode(p.pd, stream);

@@ -202,4 +202,29 @@ struct PageDecodeArgs {
 };
 cudaError_t launch_page_decode(const PageDecodeArgs& a, cudaStream_t s);
 
+// Packed-NVFP4 paged decode: one work unit per (query token, KV head) whose
+// G <= 16 query heads form the 16 rows of warp-level MMAs; each unit attends
+// over its token's own selected blocks.
+struct Fp4DecodeArgs {
+  unsigned* fault = nullptr;
+  CUtensorMap tmap_kc;  // K codes (64 bytes, 128, Hkv, pages), 64-byte swizzle, box (64, 128, 1, 1)
+  CUtensorMap tmap_vc;  // V codes, the same
+  const uint16_t* q = nullptr;  // bf16 (total_q, Hq, 128)
+  const int32_t* q2k = nullptr;  // (Hkv, total_q, topk)
+  int topk = 0;
+  const int32_t* cu_q = nullptr;
+  const int32_t* page_table = nullptr;
+  int max_pages = 0, num_pages = 0;
+  const int32_t* seqused_k = nullptr;
+  const uint8_t* k_scale = nullptr;  // (page, head) slice at p * page_stride + h * 1024
+  const uint8_t* v_scale = nullptr;
+  long long page_stride = 0;
+  int batch = 0, total_q = 0, num_qo_heads = 0, num_kv_heads = 0, G = 0;
+  float scale_log2 = 0.f;  // softmax scale * log2(e) * K global scale
+  float out_scale = 1.f;   // V global scale
+  uint16_t* out = nullptr;  // bf16 (total_q, Hq, 128)
+  float* lse = nullptr;     // (total_q, Hq) or NULL
+};
+cudaError_t launch_fp4_decode(const Fp4DecodeArgs& a, cudaStream_t s);
+
 }  // namespace msa

@@ -22,12 +22,13 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Tiled map with 128-byte swizzle over a tensor of `rank` dims (dims[0]
-// innermost, contiguous). strides_bytes[i] is the stride of dims[i+1].
-// box[0] * element size must be 128 bytes or less.
+// Tiled map over a tensor of `rank` dims (dims[0] innermost, contiguous),
+// 128-byte swizzle unless another is given. strides_bytes[i] is the stride of
+// dims[i+1]. box[0] * element size must not exceed the swizzle span.
 inline bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, const void* base,
                          const uint64_t* dims, const uint64_t* strides_bytes,
-                         const uint32_t* box) {
+                         const uint32_t* box,
+                         CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   cuuint64_t gd[5];
@@ -41,7 +42,7 @@ inline bool encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, int rank, con
     if (i + 1 < rank) gs[i] = strides_bytes[i];
   }
   CUresult r = enc(map, dt, (cuuint32_t)rank, const_cast<void*>(base), gd, gs, bx, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
