@@ -624,8 +624,8 @@ def bench_decode_nvfp4(msa, device, flush, seed=0, sqs=(1, 4), reps=7, small=Fal
                 q2k.numel() * 4 + pt.numel() * 4)
         o = torch.empty_like(inp["q"])
         lse = torch.empty(inp["q"].shape[:2], dtype=torch.float32, device=device)
-        need = msa.msa_sparse_attention_workspace_size(B, inp["q"].shape[0], inp["q"].shape[1],
-                                                       hkv, D, q2k.shape[2], sq, True)
+        need = msa.msa_sparse_attention_nvfp4_workspace_size(
+            B, inp["q"].shape[0], inp["q"].shape[1], hkv, D, q2k.shape[2], sq, pt.shape[1])
         ws = torch.empty(need, dtype=torch.uint8, device=device)
 
         def call():
@@ -665,7 +665,7 @@ def bench_decode_nvfp4(msa, device, flush, seed=0, sqs=(1, 4), reps=7, small=Fal
             "meta_bytes": int(meta),
             "roofline": {"bound": "hbm", "achieved": round(gbs_attn, 1), "peak": pk["hbm"],
                          "unit": "GB/s", "frac": round(gbs_attn / pk["hbm"], 4), "traffic": None,
-                         "kernel": "prefill_kernel<E4M3 instance, NVFP4 staging> (paged)"}}
+                         "kernel": "fp4_list_kernel + fp4_decode_kernel (paged NVFP4 decode)"}}
         del inp
         torch.cuda.empty_cache()
     out["workload"] = spec.name

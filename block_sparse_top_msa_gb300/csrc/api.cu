@@ -36,8 +36,11 @@ namespace {
 
 constexpr int kMaxTopk = 64;
 // Packed-NVFP4 calls with at most this many query tokens per request (and
-// G <= 16) take the decode kernel.
+// G <= 16) take the decode kernel when the workspace holds its lists.
 constexpr int kFp4DecodeMaxSeqQ = 16;
+bool fp4_decode_route(int num_qo_heads, int num_kv_heads, int max_seqlen_q) {
+  return num_qo_heads / num_kv_heads <= 16 && max_seqlen_q <= kFp4DecodeMaxSeqQ;
+}
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -367,8 +370,11 @@ size_t msa_sparse_attention_nvfp4_workspace_size(int batch, int total_q, int num
   const size_t base = msa_sparse_attention_workspace_size(
       batch, total_q, num_qo_heads, num_kv_heads, head_dim, topk, max_seqlen_q, 1);
   if (base == 0 || max_pages < 1) return 0;
-  if (!paged_copy_route(total_q, num_qo_heads, batch, max_pages, num_kv_heads)) return base;
-  return base + page_pool_bytes(batch, max_pages, num_kv_heads);
+  if (paged_copy_route(total_q, num_qo_heads, batch, max_pages, num_kv_heads))
+    return base + page_pool_bytes(batch, max_pages, num_kv_heads);
+  if (fp4_decode_route(num_qo_heads, num_kv_heads, max_seqlen_q))
+    return base + fp4_decode_workspace_bytes((long long)total_q * num_kv_heads, topk);
+  return base;
 }
 
 }  // extern "C"
@@ -706,11 +712,15 @@ msa_status_t build_forward_fp4(
   a.fp4_page_stride = page_stride;
   a.scale_log2 *= k_global_scale;
   a.out_scale = v_global_scale;
-  // Decode-shaped calls (G <= 16, a few query tokens per request): one unit
-  // per (token, KV head) in the register-dequantizing decode kernel.
+  // Decode-shaped calls (G <= 16, a few query tokens per request), given the
+  // workspace for their block lists: one unit per (token, KV head) in the
+  // register-dequantizing decode kernel.
   const int G = num_qo_heads / num_kv_heads;
-  if (G <= 16 && max_seqlen_q <= kFp4DecodeMaxSeqQ) {
+  const long long units = (long long)total_q * num_kv_heads;
+  if (fp4_decode_route(num_qo_heads, num_kv_heads, max_seqlen_q) && workspace != nullptr &&
+      aligned(workspace, 256) && workspace_bytes >= need + fp4_decode_workspace_bytes(units, topk)) {
     Fp4DecodeArgs& f = plan->f4;
+    place_fp4_decode_workspace(&f, static_cast<uint8_t*>(workspace) + need, units, topk);
     if (!map_fp4_codes(&f.tmap_kc, k, num_kv_heads, num_pages, page_stride) ||
         !map_fp4_codes(&f.tmap_vc, v, num_kv_heads, num_pages, page_stride))
       return MSA_CUDA_ERROR;

@@ -204,7 +204,9 @@ cudaError_t launch_page_decode(const PageDecodeArgs& a, cudaStream_t s);
 
 // Packed-NVFP4 paged decode: one work unit per (query token, KV head) whose
 // G <= 16 query heads form the 16 rows of warp-level MMAs; each unit attends
-// over its token's own selected blocks.
+// over its token's own selected blocks. A list launch writes the units' block
+// lists; the decode launch splits the list positions evenly over its CTAs.
+constexpr int kFp4DecodeMaxCtas = 1024;  // partial slots in the workspace
 struct Fp4DecodeArgs {
   unsigned* fault = nullptr;
   CUtensorMap tmap_kc;  // K codes (64 bytes, 128, Hkv, pages), 64-byte swizzle, box (64, 128, 1, 1)
@@ -224,7 +226,14 @@ struct Fp4DecodeArgs {
   float out_scale = 1.f;   // V global scale
   uint16_t* out = nullptr;  // bf16 (total_q, Hq, 128)
   float* lse = nullptr;     // (total_q, Hq) or NULL
+  // workspace (place_fp4_decode_workspace)
+  int2* list = nullptr;      // (units, topk) of (page, visible keys); page -1: none
+  int32_t* arrive = nullptr;  // (units): segments of the unit finished
+  float* part_ml = nullptr;  // (max CTAs, 2, 16, 2): a segment's (m, l) per row
+  float* part_o = nullptr;   // (max CTAs, 2, 16, 128): a segment's unnormalised O
 };
+size_t fp4_decode_workspace_bytes(long long units, int topk);
+void place_fp4_decode_workspace(Fp4DecodeArgs* a, uint8_t* ws, long long units, int topk);
 cudaError_t launch_fp4_decode(const Fp4DecodeArgs& a, cudaStream_t s);
 
 }  // namespace msa

@@ -122,9 +122,18 @@ def test_paged_copy_route_sizes(L):
     assert msa.msa_sparse_attention_nvfp4_workspace_size(*args, 128) == base + pool(2, 128, 4)
     assert msa.msa_sparse_attention_nvfp4_workspace_size(*args, 129) == base
     assert msa.msa_sparse_attention_workspace_size_kv(*args, 1, 0, 8) == base  # bf16: no copy
+    # decode-shaped (G <= 16, at most 16 query tokens per request): the block
+    # lists (units x topk of (page, keys)), one counter per unit, and the
+    # (m, l) and O partials of up to 1024 CTAs x 2 segments x 16 rows
     dec = (128, 128, 64, 4, 128, 16, 1)
+    units = 128 * 4
+    lists = r256(units * 16 * 8) + r256(units * 4) + r256(1024 * 2 * 16 * 2 * 4) + r256(
+        1024 * 2 * 16 * 128 * 4)
     assert (msa.msa_sparse_attention_nvfp4_workspace_size(*dec, 1024)
-            == msa.msa_sparse_attention_workspace_size(*dec, 1))
+            == msa.msa_sparse_attention_workspace_size(*dec, 1) + lists)
+    wide = (128, 128, 128 * 4, 4, 128, 16, 1)  # G = 128: no decode kernel
+    assert (msa.msa_sparse_attention_nvfp4_workspace_size(*wide, 1024)
+            == msa.msa_sparse_attention_workspace_size(*wide, 1))
     assert msa.msa_sparse_attention_nvfp4_workspace_size(*args, 0) == 0
 
 
