@@ -189,8 +189,14 @@ void msa_sparse_attention_plan_free(msa_attention_plan_t* plan);
  *                 max_pages * 128 * num_kv_heads), a bf16 page pool and a
  *                 renumbered page table: given that much, the pages the batch
  *                 can read are decoded to bf16 once and the attention kernel
- *                 runs on bf16 operands; otherwise it decodes NVFP4 in-kernel
- *                 (same results).
+ *                 runs on bf16 operands. For decode-shaped calls (G <= 16 and
+ *                 max_seqlen_q <= 16) it adds the per-(token, KV head) block
+ *                 lists, one merge counter per unit and fixed partial slots
+ *                 (about 17 MB): given that much, a decode kernel that
+ *                 dequantizes K and V in registers runs. With only the plain
+ *                 size the attention kernel decodes NVFP4 in-kernel (same
+ *                 results within the stated tolerance; every route computes
+ *                 S and O in fp32).
  * Unmapped pages (page id outside [0, num_pages)) are neither read nor used.
  * Returns MSA_INVALID_ARG for a NULL or misaligned pointer, a page stride not
  * a positive multiple of 16, or a global scale that is not positive and
