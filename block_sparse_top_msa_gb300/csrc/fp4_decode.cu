@@ -47,6 +47,8 @@
 // 32w + 4n + i.
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -729,14 +731,21 @@ cudaError_t launch_fp4_decode(const Fp4DecodeArgs& a, cudaStream_t s) {
   const int smem = (int)sizeof(F4Smem) + 1024;
   e = set_smem_limit((const void*)fp4_decode_kernel, smem);
   if (e != cudaSuccess) return e;
-  // Four CTAs per SM need the largest shared-memory carveout.
-  static bool carveout = false;
-  if (!carveout) {
-    e = cudaFuncSetAttribute((const void*)fp4_decode_kernel,
-                             cudaFuncAttributePreferredSharedMemoryCarveout,
-                             (int)cudaSharedmemCarveoutMaxShared);
+  // Four CTAs per SM need the largest shared-memory carveout (set once per
+  // device; a repeated set is harmless).
+  {
+    static std::atomic<unsigned long long> carveout_set{0};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    carveout = true;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if ((carveout_set.load() & bit) == 0) {
+      e = cudaFuncSetAttribute((const void*)fp4_decode_kernel,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
+      if (e != cudaSuccess) return e;
+      carveout_set.fetch_or(bit);
+    }
   }
   const long long V = units * a.topk;
   long long grid = (long long)kF4CtasPerSm * device_sm_count();

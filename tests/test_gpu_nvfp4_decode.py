@@ -199,3 +199,48 @@ def test_negative_block_scales(msa):
         region = pool[:, off:off + sc]
         region[flip] |= 0x80
     _run_and_check(msa, host, npg, hkv, "fp4dec_negative_scales")
+
+
+def test_decode_route_graph_replay(msa):
+    """The prepared decode route (list and decode launches) captured once into
+    a CUDA graph. Units are split over several CTAs each (100 units x 16 list
+    positions over the CTAs), so every replay goes through the per-unit merge
+    counters, which the list launch zeroes; each replay reads q, the pool and
+    the selection refilled in place."""
+    g = torch.Generator().manual_seed(480)
+    seqused = [int(x) for x in torch.randint(1500, 6000, (50,), generator=g)]
+    hkv = 2
+    host, npg = _inputs(g, seqused, [1] * len(seqused), 16 * hkv, hkv, 16)
+    dev = to_dev(host, DEV)
+    k, ks, v, vs = _views(dev["pool"], hkv)
+    r = msa.Nvfp4AttentionRunner(dev["q"], k, ks, v, vs, dev["q2k_indices"], dev["cu_seqlens_q"],
+                                 page_table=dev["page_table"], seqused_k=dev["seqused_k"],
+                                 k_global_scale=KGS, v_global_scale=VGS, max_seqlen_q=1,
+                                 return_softmax_lse=True)
+    r.run()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            r.run(stream=stream)
+    torch.cuda.synchronize()
+    for trial in range(3):
+        gt = torch.Generator().manual_seed(900 + trial)
+        new_pool = workloads.nvfp4_pool(npg, hkv, gt, "cpu")
+        new_q = torch.randn(host["q"].shape, generator=gt).to(torch.bfloat16)
+        new_sel = workloads.select_blocks(
+            workloads.query_positions(host["cu_seqlens_q"], seqused), hkv, 16, gt)
+        dev["pool"].copy_(new_pool)
+        dev["q"].copy_(new_q)
+        dev["q2k_indices"].copy_(new_sel)
+        graph.replay()
+        torch.cuda.synchronize()
+        fault_clear(msa)
+        kf, vf = oracle.nvfp4_dequant(new_pool, hkv, 128, KGS, VGS)
+        ref_out, ref_lse = oracle.sparse_attention(
+            new_q, kf, vf, new_sel, host["cu_seqlens_q"], causal=True,
+            page_table=host["page_table"], seqused_k=host["seqused_k"], num_pages=npg)
+        check_attention(r.out, r.lse, ref_out, ref_lse, label=f"fp4dec_graph_{trial}")
+    r.close()
