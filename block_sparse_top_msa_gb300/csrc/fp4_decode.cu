@@ -11,7 +11,7 @@
 // workspace: topk slots of (page, visible keys), the usable blocks first in
 // row order, then holes (page -1); and zeroes the unit's merge counter.
 //
-// fp4_decode_kernel: CTAs of four warps, four per SM. The units' list slots,
+// fp4_decode_kernel: CTAs of four warps, three per SM. The units' list slots,
 // taken in order, form V = units * topk positions; CTA i takes the contiguous
 // range [i V / n, (i + 1) V / n), so every CTA gets the same number of blocks
 // to within one (holes are skipped). The range cuts units into segments; a
@@ -61,7 +61,9 @@ constexpr uint32_t kOffVs = 2 * kFp4Data + kFp4Scales;   // V scales (4 x 4 tile
 constexpr uint32_t kF4StageBytes = 2 * kFp4Data + 2 * kFp4Scales;  // 18432, a multiple of 1024
 constexpr uint32_t kF4HalfBytes = kFp4Data + kFp4Scales;           // one side of a block
 constexpr int kF4Threads = 128;
-constexpr int kF4CtasPerSm = 4;
+// Three CTAs per SM (154 registers a thread, no spills) measured 4% faster
+// than four (128 registers, the compiler's cap at four).
+constexpr int kF4CtasPerSm = 3;
 constexpr int kF4Stages = 3;
 
 struct F4Smem {
@@ -731,7 +733,7 @@ cudaError_t launch_fp4_decode(const Fp4DecodeArgs& a, cudaStream_t s) {
   const int smem = (int)sizeof(F4Smem) + 1024;
   e = set_smem_limit((const void*)fp4_decode_kernel, smem);
   if (e != cudaSuccess) return e;
-  // Four CTAs per SM need the largest shared-memory carveout (set once per
+  // Several CTAs per SM need the largest shared-memory carveout (set once per
   // device; a repeated set is harmless).
   {
     static std::atomic<unsigned long long> carveout_set{0};
