@@ -71,11 +71,12 @@ struct F4Smem {
   // every warp has finished QK^T of the block, its P fragments ([k-step][lane]:
   // the A operand of one PV k-step, 4 KB) overwrite the start of the K codes.
   uint8_t stage[kF4Stages][kF4StageBytes];
+  uint16_t q[2][16 * kHeadDim];  // bf16 q rows of segment s in slot s % 2 (G rows used)
   float rmax[16][4];  // [row][warp]: per-warp block row maxima
   float lsum[16][4];  // [row][warp]: per-warp row sums at the end of a segment
   int last;           // this CTA combines the current unit's segments
   int abort;
-  uint64_t kfull[kF4Stages], vfull[kF4Stages];
+  uint64_t kfull[kF4Stages], vfull[kF4Stages], qfull[2];
 };
 
 MSA_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -297,6 +298,8 @@ __global__ void __launch_bounds__(kF4Threads, kF4CtasPerSm)
       mbar_init(&sm.kfull[s], 1);
       mbar_init(&sm.vfull[s], 1);
     }
+    mbar_init(&sm.qfull[0], 1);
+    mbar_init(&sm.qfull[1], 1);
     sm.abort = 0;
     fence_mbar_init();
   }
@@ -351,6 +354,24 @@ __global__ void __launch_bounds__(kF4Threads, kF4CtasPerSm)
   };
   if (wg == 0)
     for (int i = 0; i < kF4Stages; ++i) issue_next();
+  // q rows of segment s (unit u_first + s) into slot s % 2: segments 0 and 1
+  // up front, segment s + 1 when segment s starts (every warp has then
+  // converted segment s - 1's rows).
+  const uint32_t qbytes = (uint32_t)G * kHeadDim * 2;
+  long long nq = 0;  // segments whose q was issued (thread 0)
+  auto issue_q = [&](long long sg) {
+    const long long uu = u_first + sg;
+    const long long tq = uu / hkv, hh = uu - tq * hkv;
+    fence_async_smem();  // the slot was last read by this CTA's generic loads
+    mbar_expect_tx(&sm.qfull[sg & 1], qbytes);
+    bulk_g2s(smem_u32(sm.q[sg & 1]), a.q + ((size_t)tq * hq + (size_t)hh * G) * kHeadDim, qbytes,
+             &sm.qfull[sg & 1]);
+    nq = sg + 1;
+  };
+  if (issuer) {
+    issue_q(0);
+    if (u_last > u_first) issue_q(1);
+  }
 
   // ---- per-warp pieces of a block
   uint32_t j = 0;      // blocks consumed (the one whose S is being computed)
@@ -503,13 +524,10 @@ __global__ void __launch_bounds__(kF4Threads, kF4CtasPerSm)
   for (long long u = u_first; u <= u_last; ++u) {
     const long long p0 = max(start, u * topk), p1 = min(end, (u + 1) * topk);
     const long long tk = u / hkv, h = u - tk * hkv;
-    __syncthreads();  // every warp is past the previous segment (lsum reuse)
-    if (u + 1 <= u_last) {  // the next segment's q rows into L2
-      const long long tn = (u + 1) / hkv, hn = (u + 1) - tn * hkv;
-      if (g < G)
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(
-            a.q + ((size_t)tn * hq + (size_t)hn * G + g) * kHeadDim + 32 * c));
-    }
+    __syncthreads();  // every warp is past the previous segment (q slot, lsum reuse)
+    const long long sg = u - u_first;
+    if (issuer && sg >= 1 && u + 1 <= u_last) issue_q(sg + 1);
+    mbar_wait(&sm.qfull[sg & 1], (uint32_t)(sg >> 1) & 1u, a.fault, kFaultWaitTma, abort);
     // q rows g and g + 8 as f16 pairs scaled by 2^e per row; rs = the fp32
     // factor back to log2 units of the scaled logits.
 #pragma unroll
@@ -517,10 +535,9 @@ __global__ void __launch_bounds__(kF4Threads, kF4CtasPerSm)
       const int row = g + 8 * r;
       uint4 raw[4];
       if (row < G) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            a.q + ((size_t)tk * hq + (size_t)h * G + row) * kHeadDim + 32 * c);
 #pragma unroll
-        for (int v = 0; v < 4; ++v) raw[v] = __ldg(src + v);
+        for (int v = 0; v < 4; ++v)
+          raw[v] = lds128(smem_u32(&sm.q[sg & 1][row * kHeadDim + 32 * c + 8 * v]));
       } else {
 #pragma unroll
         for (int v = 0; v < 4; ++v) raw[v] = make_uint4(0u, 0u, 0u, 0u);
@@ -691,6 +708,10 @@ __global__ void __launch_bounds__(kF4Threads, kF4CtasPerSm)
       const uint32_t last = nis - 1 - ((nis - 1 - st) % kF4Stages);
       mbar_wait(&sm.kfull[st], (last / kF4Stages) & 1u, a.fault, kFaultWaitTma);
       mbar_wait(&sm.vfull[st], (last / kF4Stages) & 1u, a.fault, kFaultWaitTma);
+    }
+    for (long long sl = 0; sl < 2 && sl < nq; ++sl) {
+      const long long last = nq - 1 - ((nq - 1 - sl) % 2);
+      mbar_wait(&sm.qfull[sl], (uint32_t)(last >> 1) & 1u, a.fault, kFaultWaitTma);
     }
   }
 }
