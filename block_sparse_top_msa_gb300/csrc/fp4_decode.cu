@@ -21,11 +21,12 @@
 //
 // Per block, TMA brings the K and V code slices (64-byte swizzled, so every
 // shared-memory read below is conflict-free) and bulk copies bring the scale
-// slices into a two-stage ring: K of block j + 2 is issued as soon as every
-// warp has finished QK^T of block j, V of block j + 1 as soon as every warp
-// has finished PV of block j - 1 (both hold at the first barrier of block j).
-// The block is dequantized in registers on its way into the MMAs, never
-// written back:
+// slices into a three-stage ring. Inside a segment, PV of block j - 1 runs
+// together with QK^T of block j, so at the first barrier of block j every warp
+// is done with block j - 1, and block j + 2 is issued into its stage. A
+// segment's q rows arrive by bulk copy into one of two slots, one segment
+// ahead. The block is dequantized in registers on its way into the MMAs,
+// never written back:
 //   E2M1 pair -> f16 pair (cvt), times the E4M3 block scale (exact in f16:
 //   at most 6 significant bits, magnitude 2^-10 .. 2688).
 // q (bf16) enters the MMAs as f16 scaled by a power of two per row (exact for
