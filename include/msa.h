@@ -34,7 +34,7 @@ extern "C" {
 typedef enum {
   MSA_OK = 0,
   MSA_INVALID_ARG = 1,          /* malformed or conflicting arguments */
-  MSA_UNSUPPORTED = 2,          /* valid but outside this build (dtype, head_dim, sizes) */
+  MSA_UNSUPPORTED = 2,          /* valid but not supported by this library (dtype, head_dim, sizes) */
   MSA_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below the size query's answer */
   MSA_CUDA_ERROR = 4            /* a CUDA runtime/driver call failed at launch */
 } msa_status_t;
