@@ -376,11 +376,11 @@ __global__ void __launch_bounds__(kF4Threads, kF4CtasPerSm)
 
   // ---- per-warp pieces of a block
   uint32_t j = 0;      // blocks consumed (the one whose S is being computed)
-  uint32_t qa[2][16];  // q rows g, g + 8, dims 32c .. 32c + 31, f16 pairs (scaled by 2^e)
+  uint32_t qa[2][16] = {};  // q rows g, g + 8, dims 32c .. 32c + 31, f16 pairs (scaled by 2^e)
   float rs[2];         // 2^-e times the softmax scale, log2(e) and the K global scale
   float acc[4][4];     // S of this warp's 32 tokens (n-tiles of 8)
   float o[4][4];       // O of this warp's 32 dims
-  float m[2], l[2];
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
   uint4 kw[4];
   uint32_t sA[4], sB[4];
   const int grp = 2 * wg + (g >> 2);  // V scale index of dims 32 wg + 4g .. + 3
