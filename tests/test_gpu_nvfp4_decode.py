@@ -244,3 +244,18 @@ def test_decode_route_graph_replay(msa):
             page_table=host["page_table"], seqused_k=host["seqused_k"], num_pages=npg)
         check_attention(r.out, r.lse, ref_out, ref_lse, label=f"fp4dec_graph_{trial}")
     r.close()
+
+
+@pytest.mark.parametrize("case", [
+    # name, seqused, lens_q, topk
+    ("topk1", [3000, 700, 129], [1, 3, 2], 1),
+    ("sq16_max_decode_shape", [5000, 2100], [16, 16], 16),
+    # 2 units x 2 list positions: fewer positions than CTAs, so each CTA takes
+    # one position and every unit is combined from several CTAs' partials
+    ("fewer_positions_than_ctas", [900], [1], 2),
+])
+def test_small_and_boundary_shapes(msa, case):
+    name, seqused, lens_q, topk = case
+    g = torch.Generator().manual_seed(len(name) + 600)
+    host, npg = _inputs(g, seqused, lens_q, 32, 2, topk)
+    _run_and_check(msa, host, npg, 2, f"fp4dec_{name}", max_seqlen_q=max(lens_q))
